@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 SGEMM path on GB300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload square_8192]
+
+A step is one C = A * B over the whole workload (one sgemm_f32 call, one kernel
+launch).  The default workload is the compute-bound square problem
+M = N = K = 8192 with A, B ~ N(0, 1) from seed 2.  Inputs are generated on the
+host, copied to HBM once, and are larger than L2 (805 MB vs 129 MB), so no L2
+flush is needed between steps.
+
+* ``value``: TFLOP/s = 2MNK * steps * ranks / (max over ranks of the device
+  time of the K timed steps), inputs resident in HBM.
+* ``e2e``: the same metric through the public call with host buffers: each
+  step copies A and B from pinned host memory, runs sgemm_f32 and copies C back.
+* ``roofline``: the kernel is bound by the FP32 FFMA pipes.  Peak =
+  SMs x 128 FP32 lanes x 2 FLOP x clock, at the maximum SM clock (2070 MHz)
+  and, beside it, at the median clock sampled during the timed region.
+* ``cpu_baseline``: the CPU oracle (FP64 triple loop) on a bounded sample of the
+  rows of the same product, on this host's cores.
+
+Under torchrun (N > 1) each rank runs its own full replica of the product
+(one process per GPU, no collective on the data path); ``--impl reference``
+runs on rank 0 only.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "SGEMM TFLOP/s (2MNK/t) and % of FP32 roofline at M=N=K=8192"
+DEFAULT_WORKLOAD = "square_8192"
+L2_BYTES = 129e6
+FALLBACK_HBM_GBS = 6800.0
+FP32_LANES_PER_SM = 128
+MAX_SM_MHZ = 2070.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffma_tma_square_8192.md")
+KERNEL_SOURCES = ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_sgemm.cuh", "dense_fp32_matrix_04_gb300/csrc/ptx.cuh",
+                  "dense_fp32_matrix_04_gb300/csrc/tile_map.cuh"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS))
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args()
+
+
+def workload_config(name):
+    M, N, K, dist, seed = gen.WORKLOADS[name]
+    alg_bytes = 4 * (M * K + K * N + M * N)
+    return M, N, K, dist, seed, {
+        "workload": f"{name}: C = A*B, M={M} N={N} K={K}, FP32 row-major, A,B ~ "
+                    f"{'N(0,1)' if dist == 'normal' else 'uniform[-1,1]'} from seed {seed}",
+        "M": M, "N": N, "K": K,
+        "l2": (f"inputs larger than L2 ({alg_bytes / 1e6:.0f} MB of A+B+C vs 129 MB); no flush"
+               if alg_bytes > 2 * L2_BYTES else
+               f"working set {alg_bytes / 1e6:.0f} MB is within 2x L2: a 512 MB buffer is written between "
+               "timed steps (outside the per-step events)"),
+    }
+
+
+def metric_name(workload):
+    if workload == DEFAULT_WORKLOAD:
+        return METRIC
+    M, N, K = gen.WORKLOADS[workload][:3]
+    return f"SGEMM TFLOP/s (2MNK/t) and % of roofline at M={M} N={N} K={K}"
+
+
+def measured_hbm_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------- oracle legs
+
+def oracle_rows_sample(A, B, target_s):
+    """Time the CPU oracle on the first R rows of the product, R sized to ~target_s."""
+    from oracle import ref_gemm
+    M, K = A.shape
+    N = B.shape[1]
+    r = min(M, max(4, 2 * ref_gemm.num_threads()))
+    t0 = time.perf_counter()
+    ref_gemm.gemm_f64(A[:r], B, with_abs=False)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    R = int(max(1, min(M, round(r * target_s / dt))))
+    t0 = time.perf_counter()
+    ref_gemm.gemm_f64(A[:R], B, with_abs=False)
+    dt = time.perf_counter() - t0
+    return R, dt, ref_gemm.num_threads()
+
+
+def cpu_baseline(A, B, target_s):
+    M, K = A.shape
+    N = B.shape[1]
+    R, dt, cores = oracle_rows_sample(A, B, target_s)
+    tflops = 2.0 * R * N * K / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{R - 1} of C ({R}x{N}x{K}, FP64 accumulation, product only), "
+                      f"{dt:.2f} s on {cores} host threads"}
+
+
+# ---------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = (uuid or "").lower()
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < 5 and os.path.getsize(self.path) == 0:
+                time.sleep(0.05)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1].lower():
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[6:10]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        power = [num(r[4]) for r in rows if num(r[4]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][3]), "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------- ncu traffic
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel sources as they are now; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_source_digest():
+        return None
+    return int(m.group(1))
+
+
+# ---------------------------------------------------------------------- arms
+
+def kernel_name(M, N, K):
+    """The kernel sgemm_f32 launches for a contiguous M x K by K x N product."""
+    if K > 0 and K % 4 == 0 and N % 4 == 0:
+        return "sgemm_ffma_tma_kernel (256x128x32 TMA-fed tile, 3 stages, 16x8 per thread)"
+    return "sgemm_ffma_kernel (128x128x16 cp.async tile, 4 stages, 8x8 per thread)"
+
+
+def max_over_ranks(value, world, device):
+    """The largest ``value`` over all ranks (the slowest rank's time); identity for one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_step, steps, world, t_ms):
+    """Whole-job throughput: every rank runs ``steps`` full products in ``t_ms`` (the max over ranks)."""
+    return flop_per_step * steps * world / (t_ms / 1e3) / 1e12
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    M, N, K, dist, seed, cfg = workload_config(args.workload)
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    from oracle import ref_gemm
+    # size each step so that warm-up + timed steps take about 90 s in total
+    R, dt, cores = oracle_rows_sample(A, B, 90.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        ref_gemm.gemm_f64(A[:R], B, with_abs=False)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ref_gemm.gemm_f64(A[:R], B, with_abs=False)
+    t = time.perf_counter() - t0
+    value = 2.0 * R * N * K * args.steps / t / 1e12
+    sample = f"each step: rows 0..{R - 1} of C ({R}x{N}x{K}), FP64 accumulation, product only"
+    line = {
+        "impl": "reference", "metric": metric_name(args.workload), "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+        "note": "the CPU oracle (plain FP64 triple loop, OpenMP over rows) on the host cores; "
+                "the pages publish no implementation or measured number to run instead",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import dense_fp32_matrix_04_gb300 as sg
+    from dense_fp32_matrix_04_gb300 import build as sgbuild
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        sgbuild.build()
+    if world > 1:
+        dist.barrier()
+    sg.load()
+
+    M, N, K, dist_name, seed, cfg = workload_config(args.workload)
+    if world > 1:
+        cfg["parallelism"] = f"replicas x{world} (one full product per GPU, no collective)"
+    t0 = time.time()
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist_name)
+    log(f"[bench] inputs {M}x{K}, {K}x{N} generated in {time.time() - t0:.1f} s")
+    dA = torch.from_numpy(A).to(dev)
+    dB = torch.from_numpy(B).to(dev)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+
+    def step():
+        sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
+
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+
+    alg_bytes = 4 * (M * K + K * N + M * N)
+    flush = alg_bytes <= 2 * L2_BYTES
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush else None
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if not flush:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_ms = ev0.elapsed_time(ev1)
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e0, e1 in evs:
+            flush_buf.fill_(1)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    t_ms = max_over_ranks(t_ms, world, dev)
+
+    flop = 2.0 * M * N * K
+    value = job_tflops(flop, args.steps, world, t_ms)
+    per_launch_s = t_ms / args.steps / 1e3
+    peak_alu = sms * FP32_LANES_PER_SM * 2 * MAX_SM_MHZ * 1e6 / 1e12
+    hbm_gbs, hbm_src = measured_hbm_gbs()
+    t_alu = flop / (peak_alu * 1e12)
+    t_hbm = alg_bytes / (hbm_gbs * 1e9)
+    if t_alu >= t_hbm:
+        roofline = {"bound": "alu", "achieved": flop / per_launch_s / 1e12, "peak": peak_alu, "unit": "TFLOP/s",
+                    "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {MAX_SM_MHZ:.0f} MHz "
+                                  "(max SM clock)"}
+    else:
+        roofline = {"bound": "hbm", "achieved": alg_bytes / per_launch_s / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                    "peak_basis": f"copy bandwidth, {hbm_src}"}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline["traffic"] = recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None
+    roofline["algorithmic_bytes"] = alg_bytes
+    roofline["alu_floor_ms"] = t_alu * 1e3
+    roofline["hbm_floor_ms"] = t_hbm * 1e3
+    roofline["kernel"] = kernel_name(M, N, K)
+    if clocks.get("sm_mhz") and roofline["bound"] == "alu":
+        p = sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12
+        roofline["peak_at_sampled_clock"] = p
+        roofline["frac_at_sampled_clock"] = roofline["achieved"] / p
+
+    # sampled parity check of the timed output (first and last rows)
+    check = None
+    if rank == 0:
+        from oracle import ref_gemm, tolerance
+        rows = [0, M - 1]
+        C_rows = dC[rows].cpu().numpy()
+        C64, S = ref_gemm.gemm_f64(np.ascontiguousarray(A[rows]), B)
+        check = {"rows": rows, "max_error_over_bound": tolerance.max_error_ratio(C_rows, C64, S, K)}
+
+    # end to end through the public call, host buffers, copies inside the timed region
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        step()
+        hC.copy_(dC, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    te_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": job_tflops(flop, args.e2e_steps, world, te_ms), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
+           "d2h_bytes_per_step": int(hC.numel() * 4), "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(A, B, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": metric_name(args.workload), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": cfg, "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples",
+                                                                "power_w_max")},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps, "cpu_baseline": cpu,
+            "check": check, "device": props.name, "sms": sms,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,145 @@
+"""Python binding of libsgemm: FP32 C = A * B on a GB300, through the C interface
+declared in include/sgemm.h.
+
+The binding only marshals arguments: every step of the product runs in the
+library's CUDA kernels.  There is no CPU or library fallback; if the shared
+library is missing or fails to load, ``load()`` raises.
+
+* ``sgemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream=None)`` -- the C entry
+  point, with pointers given as integers or CUDA tensors (their ``data_ptr()``)
+  and the stream as a ``torch.cuda.Stream``, a raw handle or ``None`` (torch's
+  current stream on the current device).  Raises ``SgemmError`` on a non-OK
+  status.
+* ``matmul(A, B, out=None)`` -- convenience wrapper for 2-D float32 CUDA tensors
+  with unit column stride (row-major, possibly with a padded row stride).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsgemm.so")
+
+SGEMM_OK = 0
+SGEMM_ERR_INVALID_ARG = 1
+SGEMM_ERR_ALIAS = 2
+SGEMM_ERR_LAUNCH = 3
+SGEMM_ERR_DEVICE = 4
+SGEMM_ERR_TIMEOUT = 5
+
+#: Every entry point include/sgemm.h declares, with its ctypes signature.
+_SIGNATURES = {
+    "sgemm_f32": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
+    "sgemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "sgemm_version": (ctypes.c_int, []),
+    "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
+    "sgemm_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None):
+    """Load libsgemm.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libsgemm.so not built at {p}: run dense_fp32_matrix_04_gb300.build.build()")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().sgemm_status_string(int(status)).decode()
+
+
+sgemm_status_string = status_string
+
+
+def sgemm_version() -> int:
+    return int(load().sgemm_version())
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != SGEMM_OK:
+        raise SgemmError(status, where)
+
+
+def sgemm_f32(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int, stream=None) -> None:
+    """C = A * B on the GPU (see include/sgemm.h for the full contract)."""
+    lib = load()
+    st = lib.sgemm_f32(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
+                       _stream(stream))
+    _check(st, "sgemm_f32")
+
+
+def sgemm_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(load().sgemm_device_status(_stream(stream)))
+
+
+def sgemm_debug_set(flags: int, wait_limit_ns: int = 2_000_000_000) -> None:
+    """Test-only switches of the library (see include/sgemm.h)."""
+    _check(load().sgemm_debug_set(int(flags), int(wait_limit_ns)), "sgemm_debug_set")
+
+
+def _rows(t, name):
+    """Leading dimension of a row-major 2-D float32 CUDA tensor."""
+    import torch
+    if t.dim() != 2 or t.dtype != torch.float32 or not t.is_cuda:
+        raise TypeError(f"{name} must be a 2-D float32 CUDA tensor")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride (row-major)")
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def matmul(A, B, out=None, stream=None):
+    """Row-major FP32 product of two CUDA tensors via ``sgemm_f32``; returns ``out``."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    lda, ldb, ldc = _rows(A, "A"), _rows(B, "B"), _rows(out, "out")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out has the wrong shape")
+    sgemm_f32(M, N, K, A, lda, B, ldb, out, ldc, stream)
+    return out

@@ -1,0 +1,234 @@
+// TMA-fed register-tiled FP32 SGEMM for sm_103a (operands with 16-byte aligned
+// bases and leading dimensions).
+//
+// Same reuse scheme as the cp.async kernel -- block tiles staged in shared
+// memory, a multi-stage pipeline, per-thread register outer products, a
+// bank-conflict-free layout and zero-filled edges -- with the copies moved off
+// the compute threads:
+//  * One thread issues two tensor-memory-accelerator (TMA) box copies per
+//    k-step (a BM x BK box of A, a BK x BN box of B) that complete on an
+//    mbarrier; the hardware zero-fills every element outside the matrix, which
+//    is the pages' boundary masking with no per-element predicate
+//    ("SGEMM: Shared Memory Tiling Visualizer", the masked tile loads).
+//  * STAGES boxes are in flight; a stage is refilled as soon as every warp has
+//    finished reading it ("Shared Memory Tiling", 'What tiling does not fix').
+//  * A keeps its row-major layout in shared memory (rows of BK = 32 floats, 128
+//    bytes), with the TMA's 128-byte swizzle: 16-byte chunk c of row r sits at
+//    chunk c ^ (r % 8).  A thread owns rows lm, lm + 8, ... so the eight lanes
+//    that read different rows in one 16-byte load always hit eight different
+//    bank groups ("Memory hierarchy -- visual walkthrough", Step 6: padding or
+//    an equivalent permutation spreads a column across the banks).
+//  * Each thread keeps a TM x TN block of C (16 x 8 in the shipped
+//    configuration): per group of four k it loads four k-values for each of
+//    its TM rows of A (TM loads of 16 bytes), and per k a TN-wide row vector of
+//    B (TN/4 loads of 16 bytes), then does TM * TN FFMAs -- for 16 x 8, 24
+//    shared loads per 512 multiply-adds ("SGEMM: 2D Register Tiling
+//    Visualizer", 'Why this matters on real GPUs').
+//  * Lane bits are split so that every quarter-warp reads at most two distinct
+//    16-byte chunks of B (broadcast) and at most four of A.
+//  * Every wait on an mbarrier is bounded; on a timeout the CTA leaves the loop
+//    together, records an error code in device memory and writes nothing.
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "tile_map.cuh"
+
+namespace sgemm {
+
+// Tile shape: each thread owns TM rows (lm + 8 i) and TN columns (four
+// 4-column quads at ln * 4 + 16 q) of its warp's WM x WN tile; warps form a
+// WARPS_M x WARPS_N grid over the BM x BN block tile.
+// ORDER selects the FFMA order of the outer product: 0 = row-major (one A value
+// reused across a row of B values), 1 = column-major, 2 = rows in pairs.
+// G_UNROLL: how many of the BK/4 groups of four k are unrolled (code size vs
+// instruction-cache reach).
+template <int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_, int ORDER_, int MIN_BLOCKS_, int G_UNROLL_ = 8>
+struct TmaTile {
+    static constexpr int TM = TM_, TN = TN_, WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
+    static constexpr int STAGES = STAGES_, ORDER = ORDER_, MIN_BLOCKS = MIN_BLOCKS_, G_UNROLL = G_UNROLL_;
+    static constexpr int WM = 8 * TM, WN = 4 * TN;
+    static constexpr int BM = WARPS_M * WM, BN = WARPS_N * WN, BK = 32;
+    static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
+    static constexpr int A_STAGE = BM * BK * 4;  // BM swizzled rows of 128 bytes
+    static constexpr int B_STAGE = BK * BN * 4;  // BK dense rows of BN floats
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+    static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 /* alignment slack */ + 8 * STAGES /* barriers */;
+    static_assert(TN % 4 == 0, "columns come in 4-wide quads");
+    static_assert(BM <= 256 && BN <= 256, "a TMA box spans at most 256 elements per dimension");
+    static_assert(BK * 4 == 128, "A rows must be exactly one 128-byte swizzle span");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+
+// The shipped configuration: 256 x 128 block tile, 8 warps of 128 x 32, 16 x 8
+// outputs per thread in row-major FFMA order, 3 stages, k-groups unrolled by
+// two -- chosen by measurement at M = N = K = 8192 among tile shapes (8x8,
+// 8x12, 8x16, 12x8, 16x8 per thread; 128 to 512 threads), FFMA orders, stage
+// counts and unroll depths.
+using TmaMainTile = TmaTile<16, 8, 2, 4, 3, 0, 1, 2>;
+
+// Error codes written to the device error word.
+enum : int { kDeviceErrNone = 0, kDeviceErrTimeout = 1 };
+
+// Debug switches (test-only): bit 0 = never issue the TMA copies, so the
+// bounded waits run out.
+enum : int { kDebugSkipCopies = 1 };
+
+template <class T, bool VEC_C>
+__global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
+    sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
+                          int N, int K, float *__restrict__ C, int ldc, int *__restrict__ err_word,
+                          unsigned long long wait_limit_ns, int debug) {
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle pattern
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *smem = smem_raw + (base - raw);
+    const uint32_t bars = base + T::STAGES * T::STAGE;  // STAGES mbarriers of 8 bytes
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    const int tiles_m = (M + T::BM - 1) / T::BM;
+    const int tiles_n = (N + T::BN - 1) / T::BN;
+    int tile_m, tile_n;
+    grouped_tile<8>(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
+    const int m0 = tile_m * T::BM;
+    const int n0 = tile_n * T::BN;
+    const int KT = (K + T::BK - 1) / T::BK;
+
+    if (tid == 0) {
+        prefetch_tensor_map(&tmA);
+        prefetch_tensor_map(&tmB);
+#pragma unroll
+        for (int s = 0; s < T::STAGES; ++s) mbar_init(bars + 8 * s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int kt, int s) {
+        const uint32_t bar = bars + 8 * s;
+        const uint32_t dst = base + s * T::STAGE;
+        mbar_arrive_expect_tx(bar, T::STAGE);
+        tma_load_2d(dst, &tmA, kt * T::BK, m0, bar);
+        tma_load_2d(dst + T::A_STAGE, &tmB, n0, kt * T::BK, bar);
+    };
+    const bool copies = !(debug & kDebugSkipCopies);
+    if (tid == 0 && copies) {
+        const int pre = KT < T::STAGES ? KT : T::STAGES;
+        for (int s = 0; s < pre; ++s) issue(s, s);
+    }
+
+    // lane -> (lm, ln): lm from lane bits {0, 1, 3}, ln from bits {2, 4}
+    const int lm = (lane & 3) | (((lane >> 3) & 1) << 2);
+    const int ln = ((lane >> 2) & 1) | (((lane >> 4) & 1) << 1);
+    const int warp_m = warp / T::WARPS_N;
+    const int warp_n = warp % T::WARPS_N;
+    const int row0 = warp_m * T::WM + lm;          // thread rows: row0 + 8 i, i < TM
+    const int col0 = warp_n * T::WN + ln * 4;      // thread cols: col0 + 16 q + (0..3), q < TN / 4
+
+    float acc[T::TM][T::TN];
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < T::TN; ++j) acc[i][j] = 0.f;
+
+    int failed_kt = -1;
+    for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % T::STAGES;
+        const bool ok = mbar_wait_bounded(bars + 8 * s, (kt / T::STAGES) & 1, wait_limit_ns);
+        if (ok) {
+            const unsigned char *sa = smem + s * T::STAGE + row0 * 128;
+            const unsigned char *sb = smem + s * T::STAGE + T::A_STAGE + col0 * 4;
+#pragma unroll T::G_UNROLL
+            for (int g = 0; g < T::BK / 4; ++g) {
+                // four k-values for each of the 8 rows, from the swizzled chunk g ^ lm
+                const unsigned char *ag = sa + ((g ^ lm) << 4);
+                float4 a[T::TM];
+#pragma unroll
+                for (int i = 0; i < T::TM; ++i) a[i] = *reinterpret_cast<const float4 *>(ag + 1024 * i);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const unsigned char *bk = sb + (4 * g + kk) * (T::BN * 4);
+                    float b[T::TN];
+#pragma unroll
+                    for (int q = 0; q < T::TN / 4; ++q) {
+                        const float4 v = *reinterpret_cast<const float4 *>(bk + 64 * q);
+                        b[4 * q + 0] = v.x;
+                        b[4 * q + 1] = v.y;
+                        b[4 * q + 2] = v.z;
+                        b[4 * q + 3] = v.w;
+                    }
+                    float av[T::TM];
+#pragma unroll
+                    for (int i = 0; i < T::TM; ++i)
+                        av[i] = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                    if (T::ORDER == 1) {
+#pragma unroll
+                        for (int j = 0; j < T::TN; ++j)
+#pragma unroll
+                            for (int i = 0; i < T::TM; ++i) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+                    } else if (T::ORDER == 2) {
+#pragma unroll
+                        for (int i = 0; i < T::TM; i += 2)
+#pragma unroll
+                            for (int j = 0; j < T::TN; ++j) {
+                                acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+                                acc[i + 1][j] = fmaf(av[i + 1], b[j], acc[i + 1][j]);
+                            }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+                            for (int j = 0; j < T::TN; ++j) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+                    }
+                }
+            }
+        }
+        // every warp is done with stage s (or the CTA gives up together)
+        if (__syncthreads_or(!ok)) {
+            failed_kt = kt;
+            break;
+        }
+        if (tid == 0 && copies && kt + T::STAGES < KT) issue(kt + T::STAGES, s);
+    }
+
+    if (failed_kt >= 0) {
+        if (tid == 0) {
+            atomicCAS(err_word, kDeviceErrNone, kDeviceErrTimeout);
+            // let the copies already issued (k-steps failed_kt .. failed_kt + STAGES - 1)
+            // land before the CTA's shared memory is released; bounded as well
+            if (copies)
+                for (int t = failed_kt; t < KT && t < failed_kt + T::STAGES; ++t)
+                    (void)mbar_wait_bounded(bars + 8 * (t % T::STAGES), (t / T::STAGES) & 1, wait_limit_ns);
+        }
+        __syncthreads();
+        return;
+    }
+
+    // epilogue: rows row0 + 8 i, 16-byte column quads at col0 + 16 q
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i) {
+        const int row = m0 + row0 + 8 * i;
+        if (row >= M) continue;
+        float *crow = C + (int64_t)row * ldc;
+#pragma unroll
+        for (int q = 0; q < T::TN / 4; ++q) {
+            const int col = n0 + col0 + 16 * q;
+            const float *v = &acc[i][4 * q];
+            if (VEC_C && col + 3 < N) {
+                stg128(crow + col, v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < N) crow[col + j] = v[j];
+            }
+        }
+    }
+}
+
+}  // namespace sgemm

@@ -1,0 +1,105 @@
+/*
+ * libsgemm -- single-precision matrix product C = A * B on one NVIDIA GB300
+ * (sm_103a), hand-written CUDA kernels behind a plain C interface.
+ *
+ * The operation is the one the tutorial pages build step by step: every
+ * output element is the length-K dot product of a row of A and a column of B
+ * ("SGEMM: Shared Memory Tiling Visualizer", tiled kernel listing;
+ * "Shared Memory Tiling", 'The naive kernel' and 'The tiled kernel'), for
+ * general M, N, K with boundary masking (the visualizer's zero-filled tile
+ * loads) and strided row-major operands.  There is no alpha, beta or epilogue
+ * operation: C is overwritten with the product.
+ *
+ * Layout (all matrices FP32, row-major, caller-owned DEVICE memory):
+ *   A: M x K, element (i, k) at A[i * lda + k], lda >= max(1, K)
+ *   B: K x N, element (k, j) at B[k * ldb + j], ldb >= max(1, N)
+ *   C: M x N, element (i, j) at C[i * ldc + j], ldc >= max(1, N)
+ * Pointers must be 4-byte aligned; a pointer may be NULL only when its matrix
+ * has no elements.  Every call is asynchronous on `stream` (0 = the legacy
+ * default stream): the library allocates no memory, never synchronises, and
+ * does not touch host memory behind the caller's back.  Entries of C outside
+ * the M x N block (the gap between N and ldc) are never written.
+ *
+ * Numerics: each element is an FP32 sum of FP32 products in some order, with
+ * round-to-nearest fused multiply-adds; the result satisfies
+ * |C - C_exact| <= 2 * K * 2^-24 * sum_k |a_ik| |b_kj| elementwise, and is
+ * exact whenever all partial sums are exactly representable (e.g. small
+ * integers).  K == 0 writes zeros (an empty sum).
+ *
+ * Errors: every entry point validates its arguments on the host before any
+ * CUDA call and returns a status; on any status other than SGEMM_OK nothing
+ * was launched.  SGEMM_ERR_LAUNCH carries a CUDA launch failure (including a
+ * device without an sm_103a image); errors of earlier asynchronous work on the
+ * stream are not this library's and surface at the caller's next
+ * synchronisation.
+ */
+#ifndef SGEMM_H
+#define SGEMM_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1, /* negative size, short leading dimension, NULL or misaligned pointer */
+    SGEMM_ERR_ALIAS = 2,       /* C overlaps A or B */
+    SGEMM_ERR_LAUNCH = 3,      /* the CUDA launch (or its attribute set-up) failed */
+    SGEMM_ERR_DEVICE = 4,      /* the device reported an error (cudaGetDevice / attributes) */
+    SGEMM_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (reported by sgemm_device_status) */
+} sgemm_status;
+
+/*
+ * C = A * B ("Shared Memory Tiling", the tiled kernel and 'What tiling does
+ * not fix'; "SGEMM: 2D Register Tiling Visualizer", the outer-product listing).
+ * Register-tiled FP32 FFMA kernels with thread-block tiles staged in shared
+ * memory through a multi-stage pipeline:
+ *   - A and B with 16-byte aligned bases and leading dimensions (multiples of
+ *     4 floats), K >= 1: 256 x 128 block tiles copied by the tensor memory
+ *     accelerator (TMA) with hardware zero-fill at the edges, 16 x 8 outputs
+ *     per thread;
+ *   - otherwise: 128 x 128 block tiles copied by cp.async with per-element
+ *     masks, 8 x 8 outputs per thread.
+ * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
+ * The TMA kernel's waits are bounded: if a copy never lands, its blocks give
+ * up, write nothing, and the next sgemm_device_status() returns
+ * SGEMM_ERR_TIMEOUT.
+ */
+int sgemm_f32(int M, int N, int K,
+              const float *A, int lda,
+              const float *B, int ldb,
+              float *C, int ldc,
+              cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's error word, which
+ * kernels set when a bounded wait runs out.  SGEMM_OK if no kernel gave up
+ * since the last call, SGEMM_ERR_TIMEOUT if one did, SGEMM_ERR_DEVICE if a
+ * CUDA call failed (including an earlier asynchronous error on the stream).
+ */
+int sgemm_device_status(cudaStream_t stream);
+
+/*
+ * TEST-ONLY.  flags bit 0: the TMA kernel never issues its copies, so every
+ * block's bounded wait runs out (used to check the timeout path without any
+ * fault); bit 1: route every product to the cp.async kernel, so both kernels
+ * can be checked on the same inputs.  wait_limit_ns: the bound of each wait
+ * (default 2 s).  Affects every
+ * later launch in this process.  SGEMM_ERR_INVALID_ARG if flags < 0 or
+ * wait_limit_ns == 0.
+ */
+int sgemm_debug_set(int flags, unsigned long long wait_limit_ns);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *sgemm_status_string(int status);
+
+/* Library interface version: 100 * major + minor. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_H */

@@ -1,0 +1,122 @@
+"""The C interface without a GPU: the library builds for sm_103a, loads, exports
+every symbol include/sgemm.h declares, and rejects bad arguments on the host
+(status codes, no CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp32_matrix_04_gb300 as sg
+from dense_fp32_matrix_04_gb300 import build
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if h.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(sgemm_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return sg.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "sgemm_f32" in names and "sgemm_status_string" in names
+    assert len(names) == len(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in sg._SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert sg.status_string(0) == "SGEMM_OK"
+    for code in (1, 2, 3, 4, 5):
+        assert sg.status_string(code).startswith("SGEMM_ERR_")
+    assert sg.status_string(99) == "SGEMM_ERR_UNKNOWN"
+    assert sg.sgemm_version() >= 100
+
+
+def call(lib, M, N, K, A, lda, B, ldb, C, ldc):
+    return lib.sgemm_f32(M, N, K, A, lda, B, ldb, C, ldc, None)
+
+
+# fake but distinct, 16-byte aligned device-looking addresses: never dereferenced,
+# because every case below is rejected (or is empty) before any CUDA call
+PA, PB, PC = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, PA, 4, PB, 4, PC, 4),       # negative M
+    (4, -1, 4, PA, 4, PB, 4, PC, 4),       # negative N
+    (4, 4, -1, PA, 4, PB, 4, PC, 4),       # negative K
+    (4, 4, 8, PA, 7, PB, 4, PC, 4),        # lda < K
+    (4, 8, 4, PA, 4, PB, 7, PC, 8),        # ldb < N
+    (4, 8, 4, PA, 4, PB, 8, PC, 7),        # ldc < N
+    (4, 4, 4, 0, 4, PB, 4, PC, 4),         # NULL A
+    (4, 4, 4, PA, 4, 0, 4, PC, 4),         # NULL B
+    (4, 4, 4, PA, 4, PB, 4, 0, 4),         # NULL C
+    (4, 4, 4, PA + 2, 4, PB, 4, PC, 4),    # misaligned A
+    (4, 4, 4, PA, 4, PB + 1, 4, PC, 4),    # misaligned B
+    (4, 4, 4, PA, 4, PB, 4, PC + 6, 4),    # misaligned C
+    (4, 4, 0, PA, 0, PB, 4, PC, 4),        # lda must be >= 1 even for K == 0
+])
+def test_invalid_arguments_are_rejected(lib, args):
+    assert call(lib, *args) == sg.SGEMM_ERR_INVALID_ARG
+
+
+def test_aliasing_is_rejected(lib):
+    # C inside A's span
+    assert call(lib, 4, 4, 4, PA, 4, PB, 4, PA + 16, 4) == sg.SGEMM_ERR_ALIAS
+    # C's last row touches B's first element
+    assert call(lib, 4, 4, 4, PA, 4, PB, 4, PB - 4 * (3 * 4 + 3), 4) == sg.SGEMM_ERR_ALIAS
+    # adjacent but disjoint spans: C ends exactly where B starts -> passes the
+    # host checks; not launched here because it would touch the (absent) GPU
+
+
+def test_empty_output_needs_no_gpu(lib):
+    assert call(lib, 0, 5, 3, PA, 3, PB, 5, PC, 5) == sg.SGEMM_OK
+    assert call(lib, 5, 0, 3, PA, 3, PB, 1, PC, 1) == sg.SGEMM_OK
+    assert call(lib, 0, 0, 0, 0, 1, 0, 1, 0, 1) == sg.SGEMM_OK
+
+
+def test_debug_switch_validates_without_gpu(lib):
+    assert lib.sgemm_debug_set(-1, 10) == sg.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_debug_set(0, 0) == sg.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_debug_set(0, 2_000_000_000) == sg.SGEMM_OK
+
+
+def test_binding_raises_on_bad_status(lib):
+    with pytest.raises(sg.SgemmError) as e:
+        sg.sgemm_f32(-1, 1, 1, PA, 1, PB, 1, PC, 1, stream=0)
+    assert e.value.status == sg.SGEMM_ERR_INVALID_ARG
+
+
+def test_build_targets_sm_103a_only():
+    assert build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    log = open(os.path.join(build.BUILD_DIR, "ptxas.log")).read()
+    assert "sm_103a" in log
+    # no register spills in any kernel
+    assert not re.search(r"[1-9]\d* bytes spill stores", log)
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.dirname(sg.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+(oracle|gen)\b|ref_gemm|tilesim", text, flags=re.M), f
