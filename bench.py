@@ -70,6 +70,8 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--splitk", action="store_true",
+                   help="time sgemm_f32_splitk with the suggested split count (workspace allocated untimed)")
     return p.parse_args()
 
 
@@ -314,8 +316,19 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
 
-    def step():
-        sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
+    launches_per_step = 1
+    if args.splitk:
+        splits = sg.sgemm_f32_splitk_suggest(M, N, K)
+        ws_bytes = sg.sgemm_f32_splitk_workspace_size(M, N, splits)
+        ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+        launches_per_step = 2 if splits > 1 else 1
+        cfg["splitk"] = splits
+
+        def step():
+            sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
+    else:
+        def step():
+            sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
 
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
@@ -375,7 +388,8 @@ def run_ours(args):
     roofline["algorithmic_bytes"] = alg_bytes
     roofline["alu_floor_ms"] = t_alu * 1e3
     roofline["hbm_floor_ms"] = t_hbm * 1e3
-    roofline["kernel"] = kernel_name(M, N, K)
+    roofline["kernel"] = kernel_name(M, N, K) + (f" + split-K x{cfg['splitk']} with reduction"
+                                                 if cfg.get("splitk", 1) > 1 else "")
     if clocks.get("sm_mhz") and roofline["bound"] == "alu":
         p = sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["peak_at_sampled_clock"] = p
@@ -429,7 +443,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": cfg, "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples",
                                                                 "power_w_max")},
-            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps, "cpu_baseline": cpu,
+            "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * launches_per_step, "cpu_baseline": cpu,
             "check": check, "device": props.name, "sms": sms,
         }
         print(json.dumps(line), flush=True)

@@ -37,6 +37,13 @@ _SIGNATURES = {
                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "sgemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "sgemm_version": (ctypes.c_int, []),
+    "sgemm_f32_splitk": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_size_t, ctypes.c_void_p]),
+    "sgemm_f32_splitk_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "sgemm_f32_splitk_suggest": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_int)]),
     "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "sgemm_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
 }
@@ -107,6 +114,44 @@ def sgemm_f32(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int, str
     st = lib.sgemm_f32(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
                        _stream(stream))
     _check(st, "sgemm_f32")
+
+
+def sgemm_f32_splitk(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int, splits: int,
+                     workspace, workspace_bytes: int, stream=None) -> None:
+    """Split-K C = A * B with a caller-owned device workspace (include/sgemm.h)."""
+    lib = load()
+    st = lib.sgemm_f32_splitk(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
+                              int(splits), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "sgemm_f32_splitk")
+
+
+def sgemm_f32_splitk_workspace_size(M: int, N: int, splits: int) -> int:
+    return int(load().sgemm_f32_splitk_workspace_size(int(M), int(N), int(splits)))
+
+
+def sgemm_f32_splitk_suggest(M: int, N: int, K: int) -> int:
+    out = ctypes.c_int(0)
+    _check(load().sgemm_f32_splitk_suggest(int(M), int(N), int(K), ctypes.byref(out)), "sgemm_f32_splitk_suggest")
+    return int(out.value)
+
+
+def matmul_splitk(A, B, out=None, splits=None, workspace=None, stream=None):
+    """Split-K product of CUDA tensors; allocates the workspace with torch if none is given."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if splits is None:
+        splits = sgemm_f32_splitk_suggest(M, N, K)
+    need = sgemm_f32_splitk_workspace_size(M, N, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need // 4, 4), dtype=torch.float32, device=A.device)
+    lda, ldb, ldc = _rows(A, "A"), _rows(B, "B"), _rows(out, "out")
+    sgemm_f32_splitk(M, N, K, A, lda, B, ldb, out, ldc, splits, workspace, workspace.numel() * 4, stream)
+    return out
 
 
 def sgemm_device_status(stream=None) -> int:

@@ -75,7 +75,7 @@ struct FfmaTile {
 template <class T, bool VEC_B, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_kernel(int M, int N, int K, const float *__restrict__ A, int lda, const float *__restrict__ B,
-                      int ldb, float *__restrict__ C, int ldc) {
+                      int ldb, float *__restrict__ C, int ldc, float *__restrict__ partials, int ldp) {
     extern __shared__ __align__(16) float smem[];
     float *sA = smem;                          // [STAGES][BK][A_LD]
     float *sB = smem + T::STAGES * T::A_STAGE;  // [STAGES][BK][B_LD]
@@ -121,11 +121,21 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     const float *gB = B + (int64_t)b_krow0 * ldb + n0 + b_col;
     const uint32_t sB_dst = smem_addr(sB + b_krow0 * T::B_LD + b_col);
 
-    const int KT = (K + T::BK - 1) / T::BK;
+    // split-K: CTA row blockIdx.y owns k-steps [kt_begin, kt_begin + KT) and, when
+    // the grid has more than one row, writes its partial sums to its own M x N
+    // slab of `partials` (leading dimension ldp) instead of C
+    const int KT_all = (K + T::BK - 1) / T::BK;
+    const int per_split = (KT_all + gridDim.y - 1) / gridDim.y;
+    const int kt_begin = blockIdx.y * per_split;
+    const int KT = max(0, min(KT_all, kt_begin + per_split) - kt_begin);
+    if (gridDim.y > 1) {
+        C = partials + (int64_t)blockIdx.y * M * ldp;
+        ldc = ldp;
+    }
 
-    // Issue the copies of k-step `kt` into pipeline slot `slot`.
+    // Issue the copies of k-step `kt` (counted from kt_begin) into pipeline slot `slot`.
     auto load_slab = [&](int kt, int slot) {
-        const int k0 = kt * T::BK;
+        const int k0 = (kt_begin + kt) * T::BK;
         const bool full_k = k0 + T::BK <= K;
         // A
         {

@@ -80,8 +80,8 @@ enum : int { kDebugSkipCopies = 1 };
 template <class T, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
-                          int N, int K, float *__restrict__ C, int ldc, int *__restrict__ err_word,
-                          unsigned long long wait_limit_ns, int debug) {
+                          int N, int K, float *__restrict__ C, int ldc, float *__restrict__ partials, int ldp,
+                          int *__restrict__ err_word, unsigned long long wait_limit_ns, int debug) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern
     const uint32_t raw = smem_addr(smem_raw);
@@ -99,7 +99,17 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     grouped_tile<8>(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
     const int m0 = tile_m * T::BM;
     const int n0 = tile_n * T::BN;
-    const int KT = (K + T::BK - 1) / T::BK;
+    // split-K: CTA row blockIdx.y owns k-steps [kt_begin, kt_begin + KT) and, when
+    // the grid has more than one row, writes its partial sums to its own M x N
+    // slab of `partials` (leading dimension ldp) instead of C
+    const int KT_all = (K + T::BK - 1) / T::BK;
+    const int per_split = (KT_all + gridDim.y - 1) / gridDim.y;
+    const int kt_begin = blockIdx.y * per_split;
+    const int KT = max(0, min(KT_all, kt_begin + per_split) - kt_begin);
+    if (gridDim.y > 1) {
+        C = partials + (int64_t)blockIdx.y * M * ldp;
+        ldc = ldp;
+    }
 
     if (tid == 0) {
         prefetch_tensor_map(&tmA);
@@ -114,8 +124,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         const uint32_t bar = bars + 8 * s;
         const uint32_t dst = base + s * T::STAGE;
         mbar_arrive_expect_tx(bar, T::STAGE);
-        tma_load_2d(dst, &tmA, kt * T::BK, m0, bar);
-        tma_load_2d(dst + T::A_STAGE, &tmB, n0, kt * T::BK, bar);
+        tma_load_2d(dst, &tmA, (kt_begin + kt) * T::BK, m0, bar);
+        tma_load_2d(dst + T::A_STAGE, &tmB, n0, (kt_begin + kt) * T::BK, bar);
     };
     const bool copies = !(debug & kDebugSkipCopies);
     if (tid == 0 && copies) {

@@ -1,4 +1,4 @@
-// The C interface of libsgemm: argument checks, variant choice and launch.
+// The C interface of libsgemm: argument checks, kernel choice and launch.
 // Declarations and the full contract are in include/sgemm.h.
 
 #include <cuda.h>
@@ -12,6 +12,7 @@
 #include "../../include/sgemm.h"
 #include "ffma_sgemm.cuh"
 #include "ffma_tma_sgemm.cuh"
+#include "splitk_reduce.cuh"
 
 // Device error word: kernels that give up on a bounded wait record a code here;
 // sgemm_device_status() reads and clears it.  One instance per device context.
@@ -19,12 +20,12 @@ __device__ int g_sgemm_device_error;
 
 namespace {
 
-using sgemm::FfmaTile;
-
-// 128 x 128 CTA tile, 16-deep k-steps, 4 pipeline stages, 2 CTAs per SM.
-using MainTile = FfmaTile<128, 128, 16, 4, 2>;
+// 128 x 128 CTA tile, 16-deep k-steps, 4 cp.async stages, 2 CTAs per SM.
+using CpTile = sgemm::FfmaTile<128, 128, 16, 4, 2>;
+using TmaTile = sgemm::TmaMainTile;
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 64;
 
 // test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernel
 constexpr int kDebugForceCpAsync = 2;
@@ -32,6 +33,7 @@ std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 struct DeviceInfo {
+    int dev = 0;
     int sms = 0;
     int *err_word = nullptr;
 };
@@ -46,6 +48,7 @@ int device_info(DeviceInfo &out) {
     std::lock_guard<std::mutex> lock(mu);
     if (!ready[dev]) {
         DeviceInfo d;
+        d.dev = dev;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SGEMM_ERR_DEVICE;
         if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err_word), g_sgemm_device_error) != cudaSuccess)
             return SGEMM_ERR_DEVICE;
@@ -71,7 +74,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major rows x cols FP32 matrix with leading dimension ld, read in boxes of
-// box_rows x box_cols; OOB elements read as zero.
+// box_rows x box_cols; out-of-bounds elements read as zero.
 bool encode_2d(CUtensorMap *map, const float *ptr, int rows, int cols, int ld, int box_rows, int box_cols,
                CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
@@ -85,63 +88,131 @@ bool encode_2d(CUtensorMap *map, const float *ptr, int rows, int cols, int ld, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using TmaMain = sgemm::TmaMainTile;
-
-template <bool VC>
-int launch_tma(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
-               cudaStream_t stream, const DeviceInfo &info, int dev) {
-    using T = TmaMain;
-    alignas(64) CUtensorMap ta, tb;
-    if (!encode_2d(&ta, A, M, K, lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tb, B, K, N, ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return SGEMM_ERR_LAUNCH;
-    auto kernel = sgemm::sgemm_ffma_tma_kernel<T, VC>;
-    static std::atomic<int> done[kMaxDevices];
-    if (!done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
-            return SGEMM_ERR_LAUNCH;
-        done[dev].store(1, std::memory_order_release);
-    }
-    const int64_t tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
-    kernel<<<(unsigned)tiles, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, M, N, K, C, ldc, info.err_word,
-                                                                   g_wait_limit_ns.load(), g_debug_flags.load());
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
-}
-
-// Per device and per kernel instantiation: has the dynamic shared-memory limit been raised?
-template <class T, bool VB, bool VC>
-std::atomic<int> &smem_attr_done(int dev) {
-    static std::atomic<int> done[kMaxDevices];
-    return done[dev];
-}
-
-template <class T, bool VB, bool VC>
-int launch_ffma(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
-                cudaStream_t stream) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
-    auto kernel = sgemm::sgemm_ffma_kernel<T, VB, VC>;
-    std::atomic<int> &done = smem_attr_done<T, VB, VC>(dev);
-    if (!done.load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) !=
-            cudaSuccess)
-            return SGEMM_ERR_LAUNCH;
-        done.store(1, std::memory_order_release);
-    }
-    const int64_t tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
-    kernel<<<(unsigned)tiles, T::THREADS, T::SMEM_BYTES, stream>>>(M, N, K, A, lda, B, ldb, C, ldc);
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+// Raise a kernel's dynamic shared-memory limit once (per device: `done` is the
+// caller's flag for this kernel and device).
+template <class Kernel>
+bool smem_attr_once(std::atomic<int> &done, Kernel kernel, int bytes) {
+    if (done.load(std::memory_order_acquire)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done.store(1, std::memory_order_release);
+    return true;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+struct Problem {
+    int M, N, K;
+    const float *A;
+    int lda;
+    const float *B;
+    int ldb;
+    float *C;
+    int ldc;
+};
+
+// The TMA kernel needs 16-byte aligned bases and row strides and K >= 1.
+bool use_tma(const Problem &p) {
+    return p.K > 0 && aligned16(p.A) && p.lda % 4 == 0 && aligned16(p.B) && p.ldb % 4 == 0 &&
+           !(g_debug_flags.load() & kDebugForceCpAsync);
+}
+
+int k_tiles(const Problem &p) {
+    const int bk = use_tma(p) ? TmaTile::BK : CpTile::BK;
+    return (p.K + bk - 1) / bk;
+}
+
+template <class T, bool VC>
+bool tma_attr(int dev) {
+    static std::atomic<int> done[kMaxDevices];
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC>, T::SMEM_BYTES);
+}
+
+template <class T, bool VB, bool VC>
+bool cp_attr(int dev) {
+    static std::atomic<int> done[kMaxDevices];
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_kernel<T, VB, VC>, T::SMEM_BYTES);
+}
+
+// Launch the product kernel over a (tiles x splits) grid.  splits > 1 writes
+// partial sums to `partials` (splits slabs of M x ldp) instead of C.
+int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
+                   const DeviceInfo &info) {
+    const bool vc = splits > 1 || (aligned16(p.C) && p.ldc % 4 == 0);
+    if (use_tma(p)) {
+        using T = TmaTile;
+        alignas(64) CUtensorMap ta, tb;
+        if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return SGEMM_ERR_LAUNCH;
+        if (!(vc ? tma_attr<T, true>(info.dev) : tma_attr<T, false>(info.dev))) return SGEMM_ERR_LAUNCH;
+        auto kernel = vc ? sgemm::sgemm_ffma_tma_kernel<T, true> : sgemm::sgemm_ffma_tma_kernel<T, false>;
+        const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
+        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, p.C, p.ldc, partials, ldp,
+                                                            info.err_word, g_wait_limit_ns.load(),
+                                                            g_debug_flags.load());
+    } else {
+        using T = CpTile;
+        const bool vb = aligned16(p.B) && p.ldb % 4 == 0;
+        const bool attr = vb ? (vc ? cp_attr<T, true, true>(info.dev) : cp_attr<T, true, false>(info.dev))
+                             : (vc ? cp_attr<T, false, true>(info.dev) : cp_attr<T, false, false>(info.dev));
+        if (!attr) return SGEMM_ERR_LAUNCH;
+        auto kernel = vb ? (vc ? sgemm::sgemm_ffma_kernel<T, true, true> : sgemm::sgemm_ffma_kernel<T, true, false>)
+                         : (vc ? sgemm::sgemm_ffma_kernel<T, false, true> : sgemm::sgemm_ffma_kernel<T, false, false>);
+        const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
+        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc, partials,
+                                                            ldp);
+    }
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+int launch_reduce(const Problem &p, int splits, const float *partials, int ldp, cudaStream_t stream,
+                  const DeviceInfo &info) {
+    const int64_t quads = (int64_t)p.M * ((p.N + 3) / 4);
+    const int64_t want = (quads + 255) / 256;
+    const int blocks = (int)(want < (int64_t)info.sms * 8 ? want : (int64_t)info.sms * 8);
+    if (aligned16(p.C) && p.ldc % 4 == 0)
+        sgemm::splitk_reduce_kernel<true><<<blocks, 256, 0, stream>>>(p.M, p.N, splits, partials, ldp, p.C, p.ldc);
+    else
+        sgemm::splitk_reduce_kernel<false><<<blocks, 256, 0, stream>>>(p.M, p.N, splits, partials, ldp, p.C, p.ldc);
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Byte range [lo, hi) spanned by a rows x cols matrix with leading dimension ld.
-void span(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t &lo, uintptr_t &hi) {
-    lo = reinterpret_cast<uintptr_t>(p);
+void span(const void *ptr, int64_t rows, int64_t cols, int64_t ld, uintptr_t &lo, uintptr_t &hi) {
+    lo = reinterpret_cast<uintptr_t>(ptr);
     hi = (rows > 0 && cols > 0) ? lo + (uintptr_t)(((rows - 1) * ld + cols) * (int64_t)sizeof(float)) : lo;
 }
 
 bool overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Host-side checks shared by every entry point; nothing here touches the GPU.
+int validate(const Problem &p) {
+    if (p.M < 0 || p.N < 0 || p.K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (p.lda < (p.K > 1 ? p.K : 1) || p.ldb < (p.N > 1 ? p.N : 1) || p.ldc < (p.N > 1 ? p.N : 1))
+        return SGEMM_ERR_INVALID_ARG;
+    const bool a_nonempty = (int64_t)p.M * p.K > 0, b_nonempty = (int64_t)p.K * p.N > 0;
+    const bool c_nonempty = (int64_t)p.M * p.N > 0;
+    if ((a_nonempty && !p.A) || (b_nonempty && !p.B) || (c_nonempty && !p.C)) return SGEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p.A) | reinterpret_cast<uintptr_t>(p.B) | reinterpret_cast<uintptr_t>(p.C)) & 3u)
+        return SGEMM_ERR_INVALID_ARG;
+    if (!c_nonempty) return SGEMM_OK;
+    // the larger of the two tile grids must fit gridDim.x
+    const int64_t tiles = (int64_t)((p.M + CpTile::BM - 1) / CpTile::BM) * ((p.N + CpTile::BN - 1) / CpTile::BN);
+    if (tiles > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
+    uintptr_t c0, c1, a0, a1, b0, b1;
+    span(p.C, p.M, p.N, p.ldc, c0, c1);
+    span(p.A, p.M, p.K, p.lda, a0, a1);
+    span(p.B, p.K, p.N, p.ldb, b0, b1);
+    if ((a_nonempty && overlap(c0, c1, a0, a1)) || (b_nonempty && overlap(c0, c1, b0, b1))) return SGEMM_ERR_ALIAS;
+    return SGEMM_OK;
+}
+
+int ld_partials(int N) { return ((N + 3) / 4) * 4; }
+
+size_t partials_bytes(int M, int N, int splits) {
+    if (splits <= 1 || M <= 0 || N <= 0) return 0;
+    return (size_t)splits * (size_t)M * (size_t)ld_partials(N) * sizeof(float);
+}
 
 }  // namespace
 
@@ -150,8 +221,8 @@ extern "C" {
 const char *sgemm_status_string(int status) {
     switch (status) {
         case SGEMM_OK: return "SGEMM_OK";
-        case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG: bad size, leading dimension or pointer";
-        case SGEMM_ERR_ALIAS: return "SGEMM_ERR_ALIAS: C overlaps A or B";
+        case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG: bad size, leading dimension, pointer or workspace";
+        case SGEMM_ERR_ALIAS: return "SGEMM_ERR_ALIAS: C (or the workspace) overlaps another operand";
         case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: CUDA launch failed";
         case SGEMM_ERR_DEVICE: return "SGEMM_ERR_DEVICE: CUDA device query failed";
         case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a kernel gave up on a bounded wait";
@@ -159,42 +230,66 @@ const char *sgemm_status_string(int status) {
     }
 }
 
-int sgemm_version(void) { return 100; }
+int sgemm_version(void) { return 101; }
 
 int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
               cudaStream_t stream) {
-    // ---- host-side checks; nothing below touches the GPU until they pass
-    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
-    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
-    const bool a_nonempty = (int64_t)M * K > 0, b_nonempty = (int64_t)K * N > 0, c_nonempty = (int64_t)M * N > 0;
-    if ((a_nonempty && !A) || (b_nonempty && !B) || (c_nonempty && !C)) return SGEMM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 3u)
-        return SGEMM_ERR_INVALID_ARG;
-    if (!c_nonempty) return SGEMM_OK;
-    const int64_t tiles = (int64_t)((M + MainTile::BM - 1) / MainTile::BM) * ((N + MainTile::BN - 1) / MainTile::BN);
-    if (tiles > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
-    uintptr_t c0, c1, a0, a1, b0, b1;
-    span(C, M, N, ldc, c0, c1);
-    span(A, M, K, lda, a0, a1);
-    span(B, K, N, ldb, b0, b1);
-    if ((a_nonempty && overlap(c0, c1, a0, a1)) || (b_nonempty && overlap(c0, c1, b0, b1))) return SGEMM_ERR_ALIAS;
+    const Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    const int st = validate(p);
+    if (st != SGEMM_OK || (int64_t)M * N == 0) return st;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    return launch_product(p, 1, nullptr, 0, stream, info);
+}
 
-    // ---- variant
-    const bool vb = aligned16(B) && (ldb % 4 == 0);
-    const bool vc = aligned16(C) && (ldc % 4 == 0);
-    const bool va = aligned16(A) && (lda % 4 == 0);
-    if (K > 0 && va && vb && !(g_debug_flags.load() & kDebugForceCpAsync)) {
-        // TMA-fed kernel: needs 16-byte aligned bases and row strides
-        DeviceInfo info;
-        int dev = 0;
-        if (device_info(info) != SGEMM_OK || cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_DEVICE;
-        return vc ? launch_tma<true>(M, N, K, A, lda, B, ldb, C, ldc, stream, info, dev)
-                  : launch_tma<false>(M, N, K, A, lda, B, ldb, C, ldc, stream, info, dev);
+size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits) { return partials_bytes(M, N, splits); }
+
+int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits) {
+    if (!splits || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    *splits = 1;
+    if ((int64_t)M * N == 0 || K == 0) return SGEMM_OK;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    // one TMA tile per SM at a time: split until the (tiles x splits) grid
+    // fills the SMs, keeping at least four 32-deep k-steps per split
+    const int64_t tiles = (int64_t)((M + TmaTile::BM - 1) / TmaTile::BM) * ((N + TmaTile::BN - 1) / TmaTile::BN);
+    const int64_t kt = (K + TmaTile::BK - 1) / TmaTile::BK;
+    int64_t s = info.sms / (tiles > 0 ? tiles : 1);
+    if (s > kt / 4) s = kt / 4;
+    if (s > kMaxSplits) s = kMaxSplits;
+    *splits = (int)(s < 1 ? 1 : s);
+    return SGEMM_OK;
+}
+
+int sgemm_f32_splitk(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                     int splits, float *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    int st = validate(p);
+    if (st != SGEMM_OK) return st;
+    if (splits < 1 || splits > kMaxSplits) return SGEMM_ERR_INVALID_ARG;
+    if ((int64_t)M * N == 0) return SGEMM_OK;
+    // more splits than k-steps would leave empty slabs: cap at the k-step count
+    const int kt = k_tiles(p);
+    if (splits > kt) splits = kt > 0 ? kt : 1;
+    if (splits > 1) {
+        const size_t need = partials_bytes(M, N, splits);
+        if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
+        const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + need;
+        uintptr_t lo, hi;
+        span(C, M, N, ldc, lo, hi);
+        if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+        span(A, M, K, lda, lo, hi);
+        if ((int64_t)M * K > 0 && overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+        span(B, K, N, ldb, lo, hi);
+        if ((int64_t)K * N > 0 && overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
     }
-    if (vb && vc) return launch_ffma<MainTile, true, true>(M, N, K, A, lda, B, ldb, C, ldc, stream);
-    if (vb) return launch_ffma<MainTile, true, false>(M, N, K, A, lda, B, ldb, C, ldc, stream);
-    if (vc) return launch_ffma<MainTile, false, true>(M, N, K, A, lda, B, ldb, C, ldc, stream);
-    return launch_ffma<MainTile, false, false>(M, N, K, A, lda, B, ldb, C, ldc, stream);
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    if (splits == 1) return launch_product(p, 1, nullptr, 0, stream, info);
+    const int ldp = ld_partials(N);
+    st = launch_product(p, splits, workspace, ldp, stream, info);
+    if (st != SGEMM_OK) return st;
+    return launch_reduce(p, splits, workspace, ldp, stream, info);
 }
 
 int sgemm_device_status(cudaStream_t stream) {

@@ -36,6 +36,8 @@
 #ifndef SGEMM_H
 #define SGEMM_H
 
+#include <stddef.h>
+
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -72,6 +74,43 @@ int sgemm_f32(int M, int N, int K,
               const float *B, int ldb,
               float *C, int ldc,
               cudaStream_t stream);
+
+/*
+ * Split-K form of sgemm_f32 for grids with fewer output tiles than the GPU has
+ * SMs (e.g. 1024 x 1024 x 1024): the K dimension is cut into `splits` ranges
+ * of whole k-steps, each computed by its own set of thread blocks into a
+ * partial M x N product in `workspace`, and a second kernel adds the partials
+ * in increasing split order into C (deterministic; each element is still an
+ * FP32 sum of FP32 products, within the bound stated above, and exact for
+ * small-integer inputs).  The tiled kernels and their choice are those of
+ * sgemm_f32 ("Shared Memory Tiling", 'The tiled kernel': the k loop over
+ * tiles, here divided among thread blocks).
+ *   splits: 1 .. 64; values above the number of k-steps are lowered to it;
+ *           splits == 1 is exactly sgemm_f32 and needs no workspace.
+ *   workspace: caller-owned device memory of at least
+ *           sgemm_f32_splitk_workspace_size(M, N, splits) bytes, 16-byte
+ *           aligned, not overlapping A, B or C; its contents on entry do not
+ *           matter and on return are unspecified.
+ * SGEMM_ERR_INVALID_ARG for a bad split count or a missing, misaligned or
+ * short workspace; SGEMM_ERR_ALIAS if the workspace overlaps an operand.
+ */
+int sgemm_f32_splitk(int M, int N, int K,
+                     const float *A, int lda,
+                     const float *B, int ldb,
+                     float *C, int ldc,
+                     int splits, float *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/* Workspace bytes sgemm_f32_splitk needs: splits * M * (N rounded up to 4) * 4
+ * for splits > 1, else 0. */
+size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits);
+
+/*
+ * A split count for M x N x K on the current device: enough splits for the
+ * grid of 256 x 128 output tiles to reach one block per SM, with at least four
+ * 32-deep k-steps per split (1 when the tiles already fill the GPU).
+ */
+int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
 
 /*
  * Synchronises `stream`, then reads and clears this device's error word, which

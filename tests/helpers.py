@@ -10,6 +10,7 @@ from oracle import ref_gemm, tolerance
 
 CANARY_BITS = np.int32(0x7FC0_1234)   # a quiet NaN with a payload no kernel produces
 GUARD = 67                            # guard words before and after each buffer
+WS_GUARD = 64                         # guard words around a split-K workspace (keeps 16-byte alignment)
 
 
 def _device_buffer(mat, ld, offset, torch, dev):
@@ -28,9 +29,10 @@ def _device_buffer(mat, ld, offset, torch, dev):
     return buf, buf.data_ptr() + 4 * start
 
 
-def run_sgemm(sg, A, B, lda=None, ldb=None, ldc=None, a_off=0, b_off=0, c_off=0, stream=None):
-    """C = A * B through sgemm_f32; checks that nothing outside the M x N block
-    of C (guards and the row gaps between N and ldc) was written."""
+def run_sgemm(sg, A, B, lda=None, ldb=None, ldc=None, a_off=0, b_off=0, c_off=0, stream=None, splits=None):
+    """C = A * B through sgemm_f32 (or sgemm_f32_splitk when ``splits`` is given,
+    with a canary-guarded workspace); checks that nothing outside the M x N
+    block of C (guards and the row gaps between N and ldc) was written."""
     import torch
     dev = torch.device("cuda", 0)
     M, K = A.shape
@@ -42,8 +44,17 @@ def run_sgemm(sg, A, B, lda=None, ldb=None, ldc=None, a_off=0, b_off=0, c_off=0,
     b_buf, pb = _device_buffer(B, ldb, b_off, torch, dev)
     c_init = np.zeros((M, 0), np.float32)
     c_buf, pc = _device_buffer(c_init, ldc, c_off, torch, dev)
-    sg.sgemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, stream=stream)
+    ws = None
+    if splits is None:
+        sg.sgemm_f32(M, N, K, pa, lda, pb, ldb, pc, ldc, stream=stream)
+    else:
+        need = sg.sgemm_f32_splitk_workspace_size(M, N, splits)
+        ws = torch.full((need // 4 + 2 * WS_GUARD,), float("nan"), device=dev)
+        sg.sgemm_f32_splitk(M, N, K, pa, lda, pb, ldb, pc, ldc, splits, ws.data_ptr() + 4 * WS_GUARD, need, stream)
     torch.cuda.synchronize()
+    if ws is not None:
+        w = ws.cpu().numpy()
+        assert np.isnan(w[:WS_GUARD]).all() and np.isnan(w[-WS_GUARD:]).all(), "split-K wrote outside its workspace"
     host = c_buf.cpu().numpy().view(np.int32)
     start = GUARD + c_off
     C = np.empty((M, N), np.float32)

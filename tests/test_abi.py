@@ -99,6 +99,28 @@ def test_debug_switch_validates_without_gpu(lib):
     assert lib.sgemm_debug_set(0, 2_000_000_000) == sg.SGEMM_OK
 
 
+def test_splitk_workspace_size(lib):
+    assert sg.sgemm_f32_splitk_workspace_size(100, 50, 1) == 0
+    assert sg.sgemm_f32_splitk_workspace_size(100, 50, 4) == 4 * 100 * 52 * 4
+    assert sg.sgemm_f32_splitk_workspace_size(0, 50, 4) == 0
+
+
+PW = 0x7F3000000000
+
+
+@pytest.mark.parametrize("splits,ws,ws_bytes,want", [
+    (0, PW, 1 << 30, sg.SGEMM_ERR_INVALID_ARG),          # split count below 1
+    (65, PW, 1 << 30, sg.SGEMM_ERR_INVALID_ARG),         # above the maximum
+    (4, 0, 1 << 30, sg.SGEMM_ERR_INVALID_ARG),           # no workspace
+    (4, PW + 4, 1 << 30, sg.SGEMM_ERR_INVALID_ARG),      # misaligned workspace
+    (4, PW, 100, sg.SGEMM_ERR_INVALID_ARG),              # short workspace
+    (4, PA + 64, 1 << 30, sg.SGEMM_ERR_ALIAS),           # workspace over A
+])
+def test_splitk_workspace_checks_need_no_gpu(lib, splits, ws, ws_bytes, want):
+    # M = N = K = 64: every case is rejected on the host before any CUDA call
+    assert lib.sgemm_f32_splitk(64, 64, 64, PA, 64, PB, 64, PC, 64, splits, ws, ws_bytes, None) == want
+
+
 def test_binding_raises_on_bad_status(lib):
     with pytest.raises(sg.SgemmError) as e:
         sg.sgemm_f32(-1, 1, 1, PA, 1, PB, 1, PC, 1, stream=0)
