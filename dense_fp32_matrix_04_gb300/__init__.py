@@ -29,6 +29,7 @@ SGEMM_ERR_ALIAS = 2
 SGEMM_ERR_LAUNCH = 3
 SGEMM_ERR_DEVICE = 4
 SGEMM_ERR_TIMEOUT = 5
+SGEMM_ERR_SCRATCH_LIMIT = 6
 
 #: Every entry point include/sgemm.h declares, with its ctypes signature.
 _SIGNATURES = {
@@ -41,6 +42,9 @@ _SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                         ctypes.c_size_t, ctypes.c_void_p]),
+    "sgemm_f32_splitk_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "sgemm_f32_splitk_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "sgemm_f32_splitk_suggest": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_int)]),
@@ -123,6 +127,17 @@ def sgemm_f32_splitk(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: i
     st = lib.sgemm_f32_splitk(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
                               int(splits), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "sgemm_f32_splitk")
+
+
+def sgemm_f32_splitk_noalloc(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int, splits: int,
+                             stream=None) -> None:
+    """Split-K product whose partials live in the library's fixed device
+    array, for callers that cannot allocate device memory (include/sgemm.h).
+    Calls that overlap on the GPU race on that array."""
+    lib = load()
+    st = lib.sgemm_f32_splitk_noalloc(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C),
+                                      int(ldc), int(splits), _stream(stream))
+    _check(st, "sgemm_f32_splitk_noalloc")
 
 
 def sgemm_f32_splitk_workspace_size(M: int, N: int, splits: int) -> int:

@@ -18,6 +18,13 @@
 // sgemm_device_status() reads and clears it.  One instance per device context.
 __device__ int g_sgemm_device_error;
 
+// Fixed scratch for sgemm_f32_splitk_noalloc: room for the split-K partial
+// products of callers that cannot allocate device memory.  8,388,608 floats
+// (32 MiB), reserved on every device that loads this library until the
+// process exits.  Shared by all calls on a device.
+constexpr long long kNoallocScratchFloats = 8388608;
+static __device__ __align__(256) float g_splitk_noalloc_scratch[kNoallocScratchFloats];
+
 namespace {
 
 // 128 x 128 CTA tile, 16-deep k-steps, 4 cp.async stages, 2 CTAs per SM.
@@ -214,6 +221,24 @@ size_t partials_bytes(int M, int N, int splits) {
     return (size_t)splits * (size_t)M * (size_t)ld_partials(N) * sizeof(float);
 }
 
+// Device address of g_splitk_noalloc_scratch on the current device, looked up
+// once per device (the host-side name of the array is only a stand-in).
+int noalloc_scratch(float **out) {
+    static std::mutex mu;
+    static float *ptr[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        float *p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_splitk_noalloc_scratch) != cudaSuccess || !p)
+            return SGEMM_ERR_DEVICE;
+        ptr[dev] = p;
+    }
+    *out = ptr[dev];
+    return SGEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -226,6 +251,8 @@ const char *sgemm_status_string(int status) {
         case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: CUDA launch failed";
         case SGEMM_ERR_DEVICE: return "SGEMM_ERR_DEVICE: CUDA device query failed";
         case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+        case SGEMM_ERR_SCRATCH_LIMIT:
+            return "SGEMM_ERR_SCRATCH_LIMIT: splits * M * (N rounded up to 4) exceeds the 8,388,608-float static scratch";
         default: return "SGEMM_ERR_UNKNOWN";
     }
 }
@@ -290,6 +317,29 @@ int sgemm_f32_splitk(int M, int N, int K, const float *A, int lda, const float *
     st = launch_product(p, splits, workspace, ldp, stream, info);
     if (st != SGEMM_OK) return st;
     return launch_reduce(p, splits, workspace, ldp, stream, info);
+}
+
+int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C,
+                             int ldc, int splits, cudaStream_t stream) {
+    const Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    int st = validate(p);
+    if (st != SGEMM_OK) return st;
+    if (splits < 1 || splits > kMaxSplits) return SGEMM_ERR_INVALID_ARG;
+    if ((int64_t)M * N == 0) return SGEMM_OK;
+    const int kt = k_tiles(p);
+    if (splits > kt) splits = kt > 0 ? kt : 1;
+    const int ldp = ld_partials(N);
+    if (splits > 1 && (long long)splits * M * ldp > kNoallocScratchFloats) return SGEMM_ERR_SCRATCH_LIMIT;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    if (splits == 1) return launch_product(p, 1, nullptr, 0, stream, info);
+    float *scratch = nullptr;
+    if (noalloc_scratch(&scratch) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    // every (split, row < M, column < N) partial is written by the product
+    // kernel before the reduction reads it, so nothing needs clearing
+    st = launch_product(p, splits, scratch, ldp, stream, info);
+    if (st != SGEMM_OK) return st;
+    return launch_reduce(p, splits, scratch, ldp, stream, info);
 }
 
 int sgemm_device_status(cudaStream_t stream) {

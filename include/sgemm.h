@@ -50,7 +50,8 @@ typedef enum {
     SGEMM_ERR_ALIAS = 2,       /* C overlaps A or B */
     SGEMM_ERR_LAUNCH = 3,      /* the CUDA launch (or its attribute set-up) failed */
     SGEMM_ERR_DEVICE = 4,      /* the device reported an error (cudaGetDevice / attributes) */
-    SGEMM_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (reported by sgemm_device_status) */
+    SGEMM_ERR_TIMEOUT = 5,     /* a kernel gave up on a bounded wait (reported by sgemm_device_status) */
+    SGEMM_ERR_SCRATCH_LIMIT = 6 /* sgemm_f32_splitk_noalloc: the partials do not fit its static scratch */
 } sgemm_status;
 
 /*
@@ -111,6 +112,38 @@ size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits);
  * 32-deep k-steps per split (1 when the tiles already fill the GPU).
  */
 int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
+
+/*
+ * sgemm_f32_splitk without a workspace argument, for callers that cannot
+ * allocate device memory: code that runs inside a host application which owns
+ * the whole device-memory budget (a plug-in handed only its input and output
+ * buffers), or a latency-critical loop where an allocation, which may
+ * synchronise the device and take unbounded time, is not allowed.  The
+ * surveyed pages have no counterpart to this entry point; it only changes
+ * where the split-K partial products live.
+ *
+ * The partials go to one fixed array in device memory that the library
+ * reserves when it is loaded: 8,388,608 floats (32 MiB) on every device that
+ * loads the library, held until the process exits.  Requests with
+ * splits * M * (N rounded up to 4) above that (after splits is lowered to the
+ * number of k-steps) return SGEMM_ERR_SCRATCH_LIMIT and launch nothing;
+ * splits == 1 needs no scratch.  This function allocates nothing and calls no
+ * allocating routine.  Its first call on each device looks up the array's
+ * device address (a CUDA runtime query, done once per device with that device
+ * current); make that first call before any stream capture.
+ *
+ * Every call on a device shares the one array, and the array keeps the last
+ * call's partials.  Nothing in it needs to start at zero: each call writes
+ * every partial it later reads.  Calls whose kernels overlap on the GPU (on
+ * different streams, or from different threads) race on the array and give
+ * wrong results: order them on one stream or with events.  Arguments, results
+ * and the other error codes are as for sgemm_f32_splitk.
+ */
+int sgemm_f32_splitk_noalloc(int M, int N, int K,
+                             const float *A, int lda,
+                             const float *B, int ldb,
+                             float *C, int ldc,
+                             int splits, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears this device's error word, which
