@@ -70,8 +70,11 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
-    p.add_argument("--splitk", action="store_true",
-                   help="time sgemm_f32_splitk with the suggested split count (workspace allocated untimed)")
+    p.add_argument("--path", choices=["ffma", "splitk", "3xtf32"], default="ffma",
+                   help="ffma: sgemm_f32 (the headline); splitk: sgemm_f32_splitk with the suggested split "
+                        "count; 3xtf32: sgemm_f32_3xtf32 (tensor cores). Workspaces are allocated untimed.")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the extra 3xTF32 measurement reported beside the headline")
     return p.parse_args()
 
 
@@ -223,6 +226,54 @@ def recorded_traffic():
 
 # ---------------------------------------------------------------------- arms
 
+def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
+    """One step of the chosen path through the C interface; workspaces are allocated here, untimed."""
+    import torch
+    if path == "splitk":
+        splits = sg.sgemm_f32_splitk_suggest(M, N, K)
+        ws_bytes = sg.sgemm_f32_splitk_workspace_size(M, N, splits)
+        ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+        cfg["splitk"] = splits
+
+        def step():
+            sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
+        return step, (2 if splits > 1 else 1)
+    if path == "3xtf32":
+        ws_bytes = sg.sgemm_f32_3xtf32_workspace_size(M, N, K)
+        ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+        cfg["path"] = "3xtf32"
+
+        def step():
+            sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, ws_bytes, handle)
+        return step, 3
+
+    def step():
+        sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
+    return step, 1
+
+
+def tf32_peak_tflops():
+    """Dense TF32 tensor peak: the measured bf16 burst peak x the nominal TF32/bf16 ratio (1.1/2.25)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]) * 1.1 / 2.25, "measured bf16 x nominal 1.1/2.25"
+    except (OSError, KeyError, ValueError):
+        return 1900.0 * 1.1 / 2.25, "fallback bf16 1.9 PFLOP/s x nominal 1.1/2.25"
+
+
+def time_steps(step, steps, stream, dev):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1)
+
+
 def kernel_name(M, N, K):
     """The kernel sgemm_f32 launches for a contiguous M x K by K x N product."""
     if K > 0 and K % 4 == 0 and N % 4 == 0:
@@ -316,19 +367,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
 
-    launches_per_step = 1
-    if args.splitk:
-        splits = sg.sgemm_f32_splitk_suggest(M, N, K)
-        ws_bytes = sg.sgemm_f32_splitk_workspace_size(M, N, splits)
-        ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
-        launches_per_step = 2 if splits > 1 else 1
-        cfg["splitk"] = splits
-
-        def step():
-            sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
-    else:
-        def step():
-            sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
+    step, launches_per_step = make_step(sg, args.path, M, N, K, dA, dB, dC, handle, cfg, dev)
 
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
@@ -390,6 +429,15 @@ def run_ours(args):
     roofline["hbm_floor_ms"] = t_hbm * 1e3
     roofline["kernel"] = kernel_name(M, N, K) + (f" + split-K x{cfg['splitk']} with reduction"
                                                  if cfg.get("splitk", 1) > 1 else "")
+    if args.path == "3xtf32":
+        tpk, tsrc = tf32_peak_tflops()
+        roofline = {"bound": "tensor", "achieved": 3 * flop / per_launch_s / 1e12, "peak": tpk, "unit": "TFLOP/s",
+                    "peak_basis": f"dense TF32 tensor peak, {tsrc}", "traffic": None,
+                    "algorithmic_bytes": alg_bytes,
+                    "kernel": "split kernels + sgemm_3xtf32_kernel (tcgen05 kind::tf32, 128x256 tiles, 3 MMAs "
+                              "per k-slice); achieved counts the 3 TF32 products per FP32 product over the whole "
+                              "step, split passes included"}
+        roofline["frac"] = roofline["achieved"] / tpk
     if clocks.get("sm_mhz") and roofline["bound"] == "alu":
         p = sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["peak_at_sampled_clock"] = p
@@ -403,6 +451,22 @@ def run_ours(args):
         C_rows = dC[rows].cpu().numpy()
         C64, S = ref_gemm.gemm_f64(np.ascontiguousarray(A[rows]), B)
         check = {"rows": rows, "max_error_over_bound": tolerance.max_error_ratio(C_rows, C64, S, K)}
+
+    variants = []
+    if args.path == "ffma" and not args.no_variants and K > 0:
+        vstep, vl = make_step(sg, "3xtf32", M, N, K, dA, dB, dC, handle, {}, dev)
+        for _ in range(3):
+            vstep()
+        vsteps = max(5, args.steps // 2)
+        vt = max_over_ranks(time_steps(vstep, vsteps, stream, dev), world, dev)
+        tpk, tsrc = tf32_peak_tflops()
+        vval = job_tflops(flop, vsteps, world, vt)
+        variants.append({"path": "sgemm_f32_3xtf32 (tensor cores, 3xTF32 split precision)", "value": vval,
+                         "unit": "TFLOP/s", "ms_per_step": vt / vsteps, "steps": vsteps, "gpu_launches": vsteps * vl,
+                         "roofline": {"bound": "tensor", "achieved": 3 * vval / world, "peak": tpk,
+                                      "unit": "TFLOP/s", "frac": 3 * vval / world / tpk,
+                                      "peak_basis": f"dense TF32, {tsrc}",
+                                      "note": "3 TF32 products per FP32 product; split passes included"}})
 
     # end to end through the public call, host buffers, copies inside the timed region
     hA = torch.from_numpy(A).pin_memory()
@@ -444,7 +508,7 @@ def run_ours(args):
             "config": cfg, "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples",
                                                                 "power_w_max")},
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * launches_per_step, "cpu_baseline": cpu,
-            "check": check, "device": props.name, "sms": sms,
+            "check": check, "device": props.name, "sms": sms, "variants": variants,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -13,6 +13,7 @@
 #include "ffma_sgemm.cuh"
 #include "ffma_tma_sgemm.cuh"
 #include "splitk_reduce.cuh"
+#include "tf32x3_tcgen05.cuh"
 
 // Device error word: kernels that give up on a bounded wait record a code here;
 // sgemm_device_status() reads and clears it.  One instance per device context.
@@ -30,6 +31,7 @@ namespace {
 // 128 x 128 CTA tile, 16-deep k-steps, 4 cp.async stages, 2 CTAs per SM.
 using CpTile = sgemm::FfmaTile<128, 128, 16, 4, 2>;
 using TmaTile = sgemm::TmaMainTile;
+using X3Tile = sgemm::Tf32x3MainTile;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 64;
@@ -221,6 +223,47 @@ size_t partials_bytes(int M, int N, int splits) {
     return (size_t)splits * (size_t)M * (size_t)ld_partials(N) * sizeof(float);
 }
 
+// Row length of the split operands in the 3xTF32 workspace (16-byte rows for TMA).
+int64_t x3_kpad(int K) { return ((int64_t)K + 3) / 4 * 4; }
+
+size_t x3_workspace_bytes(int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return (size_t)(4 * x3_kpad(K) * (2 * (int64_t)M + 2 * (int64_t)N));
+}
+
+// The four launches of a 3xTF32 product: split A, split and transpose B, then
+// the tensor-core kernel over 128 x 256 output tiles.
+int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const DeviceInfo &info) {
+    using T = X3Tile;
+    const int64_t kp = x3_kpad(p.K);
+    float *ah = ws, *al = ws + (int64_t)p.M * kp;
+    float *bh = al + (int64_t)p.M * kp, *bl = bh + (int64_t)p.N * kp;
+    const int64_t elems = (int64_t)p.M * p.K;
+    const int64_t want = (elems + 255) / 256;
+    const int blocks = (int)(want < (int64_t)info.sms * 16 ? want : (int64_t)info.sms * 16);
+    sgemm::split_rows_tf32_kernel<<<blocks, 256, 0, stream>>>(p.M, p.K, p.A, p.lda, ah, al, (int)kp);
+    const dim3 tgrid((unsigned)((p.N + 31) / 32), (unsigned)((p.K + 31) / 32));
+    sgemm::split_transpose_tf32_kernel<<<tgrid, 256, 0, stream>>>(p.K, p.N, p.B, p.ldb, bh, bl, (int)kp);
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    alignas(64) CUtensorMap tah, tal, tbh, tbl;
+    if (!encode_2d(&tah, ah, p.M, p.K, (int)kp, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tal, al, p.M, p.K, (int)kp, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tbh, bh, p.N, p.K, (int)kp, T::BN, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tbl, bl, p.N, p.K, (int)kp, T::BN, T::BK, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SGEMM_ERR_LAUNCH;
+    const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
+    static std::atomic<int> done_v[kMaxDevices], done_s[kMaxDevices];
+    if (!(vc ? smem_attr_once(done_v[info.dev], sgemm::sgemm_3xtf32_kernel<T, true>, T::SMEM_BYTES)
+             : smem_attr_once(done_s[info.dev], sgemm::sgemm_3xtf32_kernel<T, false>, T::SMEM_BYTES)))
+        return SGEMM_ERR_LAUNCH;
+    auto kernel = vc ? sgemm::sgemm_3xtf32_kernel<T, true> : sgemm::sgemm_3xtf32_kernel<T, false>;
+    const unsigned tiles = (unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN));
+    kernel<<<tiles, T::THREADS, T::SMEM_BYTES, stream>>>(tah, tal, tbh, tbl, p.M, p.N, p.K, p.C, p.ldc,
+                                                         info.err_word, g_wait_limit_ns.load(),
+                                                         g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Device address of g_splitk_noalloc_scratch on the current device, looked up
 // once per device (the host-side name of the array is only a stand-in).
 int noalloc_scratch(float **out) {
@@ -340,6 +383,30 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const
     st = launch_product(p, splits, scratch, ldp, stream, info);
     if (st != SGEMM_OK) return st;
     return launch_reduce(p, splits, scratch, ldp, stream, info);
+}
+
+size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K) { return x3_workspace_bytes(M, N, K); }
+
+int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                     float *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    const int st = validate(p);
+    if (st != SGEMM_OK || (int64_t)M * N == 0) return st;
+    if (K > 65535 * 32) return SGEMM_ERR_INVALID_ARG;
+    if (K == 0) return sgemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream);  // an empty sum: zeros
+    const size_t need = x3_workspace_bytes(M, N, K);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + need;
+    uintptr_t lo, hi;
+    span(C, M, N, ldc, lo, hi);
+    if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+    span(A, M, K, lda, lo, hi);
+    if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+    span(B, K, N, ldb, lo, hi);
+    if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    return launch_3xtf32(p, workspace, stream, info);
 }
 
 int sgemm_device_status(cudaStream_t stream) {

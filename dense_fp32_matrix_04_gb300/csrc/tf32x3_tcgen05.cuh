@@ -1,0 +1,246 @@
+// 3xTF32 SGEMM on the 5th-generation tensor cores (tcgen05, accumulator in
+// TMEM) for sm_103a: C = A * B in FP32 accuracy from TF32 products.
+//
+// Each FP32 operand is split once, in HBM, into a TF32 "high" part and a TF32
+// "low" part, a = a_hi + a_lo + e with a_hi = rna_tf32(a),
+// a_lo = rna_tf32(a - a_hi) and |e| <= 2^-22 |a| (a - a_hi is exact in FP32).
+// The product keeps the three largest cross terms,
+//     C = A_hi B_hi + A_hi B_lo + A_lo B_hi,
+// dropping A_lo B_lo (< 2^-22 |a||b|), so each product carries a relative
+// error of about 3 * 2^-22 before the FP32 accumulation.  Small integers have
+// a_lo = 0 and stay exact.
+//
+// The matrix product itself is the tiled scheme of the pages ("Shared Memory
+// Tiling", the tiled kernel; "SGEMM: Shared Memory Tiling Visualizer", the
+// masked tile loads) with the inner-product loop moved onto the tensor cores:
+//  * TMA copies 128 x 32 boxes of A_hi, A_lo and 256 x 32 boxes of B_hi^T,
+//    B_lo^T (all K-major, 128-byte swizzled) into a STAGES-deep ring,
+//    zero-filling outside the matrices (the boundary masking);
+//  * one thread issues, per 32-deep k-step, 3 products x 4 tcgen05.mma of
+//    128 x 256 x 8 into one FP32 accumulator of 128 lanes x 256 columns in
+//    TMEM, and commits each stage back to the copy thread once the tensor
+//    cores have read it (the pipelining of 'What tiling does not fix');
+//  * four warps then read the accumulator out of TMEM (each warp its 32
+//    lanes) and store the 128 x 256 tile of C with masks.
+// Every mbarrier wait is bounded; a CTA that gives up writes nothing, records
+// an error code in device memory and still frees its TMEM.
+#pragma once
+
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "tile_map.cuh"
+
+namespace sgemm {
+
+// ---------------------------------------------------------------- operand split (memory-bound)
+
+// hi[i][k], lo[i][k] (leading dimension ldo) from the M x K matrix A.
+__global__ void __launch_bounds__(256) split_rows_tf32_kernel(int M, int K, const float *__restrict__ A, int lda,
+                                                              float *__restrict__ hi, float *__restrict__ lo,
+                                                              int ldo) {
+    const int64_t total = (int64_t)M * K;
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = t / K;
+        const int64_t k = t - i * K;
+        const float a = A[i * lda + k];
+        const float h = to_tf32_rna(a);
+        hi[i * ldo + k] = h;
+        lo[i * ldo + k] = to_tf32_rna(a - h);
+    }
+}
+
+// hi_t[j][k], lo_t[j][k] (leading dimension ldo): the split of the K x N matrix
+// B, transposed to N x K through a padded 32 x 33 shared tile.
+__global__ void __launch_bounds__(256) split_transpose_tf32_kernel(int K, int N, const float *__restrict__ B, int ldb,
+                                                                   float *__restrict__ hi_t, float *__restrict__ lo_t,
+                                                                   int ldo) {
+    __shared__ float th[32][33];
+    __shared__ float tl[32][33];
+    const int n0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int kk = ty + 8 * r;
+        if (k0 + kk < K && n0 + tx < N) {
+            const float b = B[(int64_t)(k0 + kk) * ldb + n0 + tx];
+            const float h = to_tf32_rna(b);
+            th[kk][tx] = h;
+            tl[kk][tx] = to_tf32_rna(b - h);
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int nn = ty + 8 * r;
+        if (n0 + nn < N && k0 + tx < K) {
+            hi_t[(int64_t)(n0 + nn) * ldo + k0 + tx] = th[tx][nn];
+            lo_t[(int64_t)(n0 + nn) * ldo + k0 + tx] = tl[tx][nn];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- tensor-core product
+
+template <int BN_, int STAGES_>
+struct Tf32x3Tile {
+    static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
+    static constexpr int THREADS = 128;           // 4 warps: copies (warp 0), MMA (warp 1), all 4 drain TMEM
+    static constexpr int UMMA_K = 8;              // TF32 elements per tcgen05.mma
+    static constexpr int A_BYTES = BM * BK * 4;   // one operand box: 128 rows of 128 bytes
+    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;  // A_hi, A_lo, B_hi^T, B_lo^T
+    static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 /* alignment */ + 256 /* barriers, flags */;
+    static constexpr int TMEM_COLS = BN;          // FP32 accumulator: 128 lanes x BN columns
+    static constexpr int SBO = 8 * 128;           // bytes between 8-row groups of a 128-byte-swizzled box
+    // instruction descriptor: D = F32 (bits 4-5 = 1), A = B = TF32 (bits 7-9, 10-12 = 2),
+    // both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
+    static constexpr uint32_t IDESC =
+        (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation: power of two >= 32");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+
+// Shared-memory matrix descriptor for a K-major operand stored in 128-byte
+// swizzled rows (the layout the TMA's 128-byte swizzle writes): start address,
+// leading-byte offset (unused for this layout, set to 1), stride-byte offset
+// between 8-row groups, descriptor version 1 (bit 46), swizzle mode 2.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+template <class T, bool VEC_C>
+__global__ void __launch_bounds__(T::THREADS, 1)
+    sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
+                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M,
+                        int N, int K, float *__restrict__ C, int ldc, int *__restrict__ err_word,
+                        unsigned long long wait_limit_ns, int debug) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *smem = smem_raw + (base - raw);
+    const uint32_t bars = base + T::STAGES * T::STAGE;         // full[S], empty[S], done
+    const uint32_t full0 = bars, empty0 = bars + 8 * T::STAGES, done_bar = bars + 16 * T::STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + T::STAGES * T::STAGE + 16 * T::STAGES + 8);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::STAGES * T::STAGE + 16 * T::STAGES + 16);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles_m = (M + T::BM - 1) / T::BM, tiles_n = (N + T::BN - 1) / T::BN;
+    int tile_m, tile_n;
+    grouped_tile<8>(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
+    const int m0 = tile_m * T::BM, n0 = tile_n * T::BN;
+    const int KT = (K + T::BK - 1) / T::BK;
+
+    if (warp == 0) {
+        tmem_alloc(smem_addr(tmem_slot), T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- copies: fill stage kt % STAGES once the tensor cores have read its previous contents
+        prefetch_tensor_map(&tmAh);
+        prefetch_tensor_map(&tmAl);
+        prefetch_tensor_map(&tmBh);
+        prefetch_tensor_map(&tmBl);
+        const bool copies = !(debug & 1);
+        int issued = 0;
+        for (int kt = 0; copies && kt < KT; ++kt) {
+            const int s = kt % T::STAGES, use = kt / T::STAGES;
+            if (use > 0 && !mbar_wait_bounded(empty0 + 8 * s, (use - 1) & 1, wait_limit_ns)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            const uint32_t dst = base + s * T::STAGE, bar = full0 + 8 * s;
+            mbar_arrive_expect_tx(bar, T::STAGE);
+            tma_load_2d(dst, &tmAh, kt * T::BK, m0, bar);
+            tma_load_2d(dst + T::A_BYTES, &tmAl, kt * T::BK, m0, bar);
+            tma_load_2d(dst + 2 * T::A_BYTES, &tmBh, kt * T::BK, n0, bar);
+            tma_load_2d(dst + 2 * T::A_BYTES + T::B_BYTES, &tmBl, kt * T::BK, n0, bar);
+            issued = kt + 1;
+        }
+        if (*abort_flag) {
+            // let the copies still in flight land before shared memory is released (bounded)
+            for (int t = issued - T::STAGES > 0 ? issued - T::STAGES : 0; t < issued; ++t)
+                (void)mbar_wait_bounded(full0 + 8 * (t % T::STAGES), (t / T::STAGES) & 1, wait_limit_ns);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- tensor cores: D = A_hi B_hi + A_hi B_lo + A_lo B_hi over all k-steps
+        for (int kt = 0; kt < KT; ++kt) {
+            const int s = kt % T::STAGES, use = kt / T::STAGES;
+            if (!mbar_wait_bounded(full0 + 8 * s, use & 1, wait_limit_ns)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t ah = base + s * T::STAGE, al = ah + T::A_BYTES;
+            const uint32_t bh = ah + 2 * T::A_BYTES, bl = bh + T::B_BYTES;
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+                const uint32_t a = p == 2 ? al : ah;
+                const uint32_t b = p == 1 ? bl : bh;
+#pragma unroll
+                for (int kk = 0; kk < T::BK / T::UMMA_K; ++kk) {
+                    const uint64_t da = umma_desc_sw128(a + kk * T::UMMA_K * 4, T::SBO);
+                    const uint64_t db = umma_desc_sw128(b + kk * T::UMMA_K * 4, T::SBO);
+                    umma_tf32(tmem, da, db, T::IDESC, (kt | p | kk) != 0);
+                }
+            }
+            umma_commit(empty0 + 8 * s);  // stage s may be refilled once these MMAs have read it
+        }
+        umma_commit(done_bar);  // the accumulator is final once every MMA above is done
+    }
+
+    // ---- all warps: wait for the accumulator, drain TMEM, store the tile
+    __syncwarp();
+    const bool ready = mbar_wait_bounded(done_bar, 0, wait_limit_ns);
+    const bool ok = __all_sync(0xffffffffu, ready && *abort_flag == 0);
+    tc_fence_after_sync();
+    if (ok) {
+        const int row = m0 + 32 * warp + lane;
+        float *crow = C + (int64_t)row * ldc;
+#pragma unroll 1
+        for (int c0 = 0; c0 < T::BN; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+            if (row < M) {
+                const int col = n0 + c0;
+                if (VEC_C && col + 31 < N) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) stg128(crow + col + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col + j < N) crow[col + j] = v[j];
+                }
+            }
+        }
+    } else if (tid == 0) {
+        atomicCAS(err_word, 0, 1);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, T::TMEM_COLS);
+}
+
+// Shipped configuration: 128 x 256 output tiles, two 96 KiB stages.
+using Tf32x3MainTile = Tf32x3Tile<256, 2>;
+
+}  // namespace sgemm

@@ -114,6 +114,40 @@ size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits);
 int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
 
 /*
+ * C = A * B in FP32 accuracy on the tensor cores ("3xTF32").  Each operand is
+ * split into a TF32 high part and a TF32 low part (rounded to nearest), and
+ * C = A_hi B_hi + A_hi B_lo + A_lo B_hi is accumulated in FP32 by tcgen05
+ * matrix instructions with the accumulator in tensor memory.  The tiling,
+ * pipelining and edge masking are those of the tiled kernel ("Shared Memory
+ * Tiling", the tiled kernel and 'What tiling does not fix'), with the inner
+ * product on the tensor cores instead of the FP32 cores.
+ *
+ * Accuracy: each product carries a relative error of about 3 * 2^-22 from the
+ * split, on top of the FP32 accumulation; the result is held to the same bound
+ * as sgemm_f32, |C - C_exact| <= 2 K 2^-24 sum_k |a_ik| |b_kj|, which this
+ * leaves room for once K is a few dozen (tested at K = 9 and up).  Small
+ * integers are split exactly (A_lo = 0), so integer products whose partial
+ * sums stay below 2^24 are exact.
+ *
+ * workspace: caller-owned device memory of at least
+ * sgemm_f32_3xtf32_workspace_size(M, N, K) bytes, 16-byte aligned, not
+ * overlapping A, B or C; it receives A_hi, A_lo (M x K) and B_hi, B_lo
+ * transposed (N x K), with rows padded to a multiple of 4 floats.  Any
+ * alignment of A, B and C is accepted.  K <= 2,097,120.  K == 0 writes zeros
+ * and needs no workspace.  Errors as for sgemm_f32_splitk; the copy waits are
+ * bounded and report through sgemm_device_status.
+ */
+int sgemm_f32_3xtf32(int M, int N, int K,
+                     const float *A, int lda,
+                     const float *B, int ldb,
+                     float *C, int ldc,
+                     float *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/* Workspace bytes sgemm_f32_3xtf32 needs: 4 * (2M + 2N) * (K rounded up to 4). */
+size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K);
+
+/*
  * sgemm_f32_splitk without a workspace argument, for callers that cannot
  * allocate device memory: code that runs inside a host application which owns
  * the whole device-memory budget (a plug-in handed only its input and output
@@ -154,7 +188,7 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K,
 int sgemm_device_status(cudaStream_t stream);
 
 /*
- * TEST-ONLY.  flags bit 0: the TMA kernel never issues its copies, so every
+ * TEST-ONLY.  flags bit 0: the TMA-fed kernels never issue their copies, so every
  * block's bounded wait runs out (used to check the timeout path without any
  * fault); bit 1: route every product to the cp.async kernel, so both kernels
  * can be checked on the same inputs.  wait_limit_ns: the bound of each wait

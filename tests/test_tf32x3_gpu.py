@@ -1,0 +1,143 @@
+"""Parity of the 3xTF32 tensor-core product (sgemm_f32_3xtf32) with the FP64
+oracle under the same bound as the FP32 kernels, |C - C64| <= 2 K u sum|a||b|,
+and exactly for small integers; plus workspace handling and the bounded-wait
+timeout path of the tcgen05 kernel."""
+
+import numpy as np
+import pytest
+
+import gen
+from helpers import CANARY_BITS, GUARD, WS_GUARD, _device_buffer, check_entries, check_full, check_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sg(cuda_device, lib):
+    import dense_fp32_matrix_04_gb300 as sg
+    sg.sgemm_device_status()
+    return sg
+
+
+def run_x3(sg, A, B, lda=None, ldb=None, ldc=None, a_off=0, b_off=0, c_off=0):
+    """C = A * B through sgemm_f32_3xtf32 with canaries around C and the workspace."""
+    import torch
+    dev = torch.device("cuda", 0)
+    M, K = A.shape
+    N = B.shape[1]
+    lda, ldb, ldc = lda or max(K, 1), ldb or max(N, 1), ldc or max(N, 1)
+    a_buf, pa = _device_buffer(A, lda, a_off, torch, dev)
+    b_buf, pb = _device_buffer(B, ldb, b_off, torch, dev)
+    c_buf, pc = _device_buffer(np.zeros((M, 0), np.float32), ldc, c_off, torch, dev)
+    need = sg.sgemm_f32_3xtf32_workspace_size(M, N, K)
+    ws = torch.full((need // 4 + 2 * WS_GUARD,), float("nan"), device=dev)
+    sg.sgemm_f32_3xtf32(M, N, K, pa, lda, pb, ldb, pc, ldc, ws.data_ptr() + 4 * WS_GUARD, need)
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    w = ws.cpu().numpy()
+    assert np.isnan(w[:WS_GUARD]).all() and np.isnan(w[-WS_GUARD:]).all(), "wrote outside the workspace"
+    host = c_buf.cpu().numpy().view(np.int32)
+    start = GUARD + c_off
+    C = np.empty((M, N), np.float32)
+    touched = np.zeros(host.size, bool)
+    for r in range(M):
+        C[r] = host[start + r * ldc: start + r * ldc + N].view(np.float32)
+        touched[start + r * ldc: start + r * ldc + N] = True
+    assert np.all(host[~touched] == CANARY_BITS), "wrote outside the M x N block of C"
+    return C
+
+
+def test_one_tile(sg):
+    A, B = gen.operands(128, 256, 32, seed=70)
+    check_full(run_x3(sg, A, B), A, B)
+
+
+def test_integer_exact(sg):
+    A = gen.matrix(71, gen.STREAM_A_INT, 300, 1000, "int")
+    B = gen.matrix(71, gen.STREAM_B_INT, 1000, 257, "int")
+    check_full(run_x3(sg, A, B), A, B, exact=True)
+
+
+def test_tiny_6x6x9(sg):
+    A, B = gen.operands(6, 6, 9, seed=0)
+    check_full(run_x3(sg, A, B), A, B)
+    Ai, Bi = gen.operands(6, 6, 9, seed=0, integer_copy=True)
+    check_full(run_x3(sg, Ai, Bi), Ai, Bi, exact=True)
+
+
+def test_square_1024(sg):
+    A, B = gen.operands(1024, 1024, 1024, seed=1)
+    check_full(run_x3(sg, A, B), A, B)
+
+
+def test_identity_exact_on_tf32_values(sg):
+    # an identity times a matrix of TF32-representable values is exact
+    A = gen.matrix(72, gen.STREAM_A_INT, 200, 160, "int") / np.float32(8)
+    I = np.eye(160, dtype=np.float32)
+    assert np.array_equal(run_x3(sg, A.astype(np.float32), I), A)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 5, 33), (129, 257, 31), (200, 300, 100), (130, 513, 257),
+                                   (256, 256, 512)])
+def test_ragged_shapes(sg, M, N, K):
+    A, B = gen.operands(M, N, K, seed=73)
+    check_full(run_x3(sg, A, B), A, B)
+
+
+def test_strides_and_unaligned_pointers(sg):
+    A, B = gen.operands(150, 140, 100, seed=74)
+    check_full(run_x3(sg, A, B, lda=103, ldb=141, ldc=147, a_off=1, b_off=3, c_off=2), A, B)
+
+
+def test_deterministic(sg):
+    A, B = gen.operands(333, 444, 555, seed=75)
+    assert np.array_equal(run_x3(sg, A, B), run_x3(sg, A, B))
+
+
+def _device_x3(sg, A, B):
+    import torch
+    C = sg.matmul_3xtf32(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    return C.cpu().numpy()
+
+
+def test_ragged_3001x4999x2047(sg):
+    M, N, K, dist, seed = gen.WORKLOADS["ragged_3001x4999x2047"]
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    C = _device_x3(sg, A, B)
+    check_rows(C, A, B, [0, 1, 127, 128, 2999, 3000] + list(np.random.default_rng(3).integers(0, M, 20)))
+
+
+def test_square_8192_sampled(sg):
+    M, N, K, dist, seed = gen.WORKLOADS["square_8192"]
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    C = _device_x3(sg, A, B)
+    assert np.isfinite(C).all()
+    check_rows(C, A, B, [0, 127, 128, 4095, 8191])
+    rng = np.random.default_rng(6)
+    check_entries(C, A, B, rng.integers(0, M, 2000), rng.integers(0, N, 2000))
+
+
+def test_skinny_sampled(sg):
+    M, N, K, dist, seed = gen.WORKLOADS["skinny_16384x16384x32"]
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    C = _device_x3(sg, A, B)
+    check_rows(C, A, B, [0, 16383] + list(np.random.default_rng(7).integers(0, M, 10)))
+
+
+def test_timeout_path(sg):
+    import torch
+    A, B = gen.operands(128, 256, 64, seed=76)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(np.full((128, 256), CANARY_BITS, np.int32).view(np.float32)).cuda()
+    need = sg.sgemm_f32_3xtf32_workspace_size(128, 256, 64)
+    ws = torch.empty(need // 4, device="cuda")
+    try:
+        sg.sgemm_debug_set(1, 50_000_000)
+        sg.sgemm_f32_3xtf32(128, 256, 64, dA, 64, dB, 256, dC, 256, ws, need)
+        assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
+        assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
+    finally:
+        sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_f32_3xtf32(128, 256, 64, dA, 64, dB, 256, dC, 256, ws, need)
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    check_full(dC.cpu().numpy(), A, B)
