@@ -238,18 +238,21 @@ int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const Device
     const int64_t kp = x3_kpad(p.K);
     float *ah = ws, *al = ws + (int64_t)p.M * kp;
     float *bh = al + (int64_t)p.M * kp, *bl = bh + (int64_t)p.N * kp;
-    const int64_t elems = (int64_t)p.M * p.K;
-    const int64_t want = (elems + 255) / 256;
-    const int blocks = (int)(want < (int64_t)info.sms * 16 ? want : (int64_t)info.sms * 16);
-    sgemm::split_rows_tf32_kernel<<<blocks, 256, 0, stream>>>(p.M, p.K, p.A, p.lda, ah, al, (int)kp);
+    const int quads = (p.K + 3) / 4;
+    const dim3 rgrid((unsigned)((quads + 255) / 256), (unsigned)(p.M < 65535 ? p.M : 65535));
+    if (aligned16(p.A) && p.lda % 4 == 0)
+        sgemm::split_rows_tf32_kernel<true><<<rgrid, 256, 0, stream>>>(p.M, p.K, p.A, p.lda, ah, al, (int)kp);
+    else
+        sgemm::split_rows_tf32_kernel<false><<<rgrid, 256, 0, stream>>>(p.M, p.K, p.A, p.lda, ah, al, (int)kp);
     const dim3 tgrid((unsigned)((p.N + 31) / 32), (unsigned)((p.K + 31) / 32));
     sgemm::split_transpose_tf32_kernel<<<tgrid, 256, 0, stream>>>(p.K, p.N, p.B, p.ldb, bh, bl, (int)kp);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     alignas(64) CUtensorMap tah, tal, tbh, tbl;
-    if (!encode_2d(&tah, ah, p.M, p.K, (int)kp, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tal, al, p.M, p.K, (int)kp, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tbh, bh, p.N, p.K, (int)kp, T::BN, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tbl, bl, p.N, p.K, (int)kp, T::BN, T::BK, CU_TENSOR_MAP_SWIZZLE_128B))
+    const CUtensorMapSwizzle sw = T::ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_2d(&tah, ah, p.M, p.K, (int)kp, T::BM, T::BK, sw) ||
+        !encode_2d(&tal, al, p.M, p.K, (int)kp, T::BM, T::BK, sw) ||
+        !encode_2d(&tbh, bh, p.N, p.K, (int)kp, T::BN, T::BK, sw) ||
+        !encode_2d(&tbl, bl, p.N, p.K, (int)kp, T::BN, T::BK, sw))
         return SGEMM_ERR_LAUNCH;
     const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
     static std::atomic<int> done_v[kMaxDevices], done_s[kMaxDevices];

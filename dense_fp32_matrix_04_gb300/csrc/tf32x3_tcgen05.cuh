@@ -13,15 +13,15 @@
 // The matrix product itself is the tiled scheme of the pages ("Shared Memory
 // Tiling", the tiled kernel; "SGEMM: Shared Memory Tiling Visualizer", the
 // masked tile loads) with the inner-product loop moved onto the tensor cores:
-//  * TMA copies 128 x 32 boxes of A_hi, A_lo and 256 x 32 boxes of B_hi^T,
-//    B_lo^T (all K-major, 128-byte swizzled) into a STAGES-deep ring,
+//  * TMA copies 128 x BK boxes of A_hi, A_lo and BN x BK boxes of B_hi^T,
+//    B_lo^T (all K-major, 128- or 64-byte swizzled) into a STAGES-deep ring,
 //    zero-filling outside the matrices (the boundary masking);
-//  * one thread issues, per 32-deep k-step, 3 products x 4 tcgen05.mma of
-//    128 x 256 x 8 into one FP32 accumulator of 128 lanes x 256 columns in
+//  * one thread issues, per BK-deep k-step, 3 products x BK/8 tcgen05.mma of
+//    128 x BN x 8 into one FP32 accumulator of 128 lanes x BN columns in
 //    TMEM, and commits each stage back to the copy thread once the tensor
 //    cores have read it (the pipelining of 'What tiling does not fix');
 //  * four warps then read the accumulator out of TMEM (each warp its 32
-//    lanes) and store the 128 x 256 tile of C with masks.
+//    lanes) and store the 128 x BN tile of C with masks.
 // Every mbarrier wait is bounded; a CTA that gives up writes nothing, records
 // an error code in device memory and still frees its TMEM.
 #pragma once
@@ -37,18 +37,35 @@ namespace sgemm {
 
 // ---------------------------------------------------------------- operand split (memory-bound)
 
-// hi[i][k], lo[i][k] (leading dimension ldo) from the M x K matrix A.
+// hi[i][k], lo[i][k] (leading dimension ldo, a multiple of 4, 16-byte aligned
+// rows) from the M x K matrix A.  Each thread splits a quad of 4 columns: one
+// 16-byte load when A's rows allow it (VEC_A), 4-byte loads otherwise, and one
+// 16-byte store of each part; columns K .. ldo-1 of the output are written as
+// zeros.  Grid: x over quads of columns, y (strided) over rows.
+template <bool VEC_A>
 __global__ void __launch_bounds__(256) split_rows_tf32_kernel(int M, int K, const float *__restrict__ A, int lda,
                                                               float *__restrict__ hi, float *__restrict__ lo,
                                                               int ldo) {
-    const int64_t total = (int64_t)M * K;
-    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = t / K;
-        const int64_t k = t - i * K;
-        const float a = A[i * lda + k];
-        const float h = to_tf32_rna(a);
-        hi[i * ldo + k] = h;
-        lo[i * ldo + k] = to_tf32_rna(a - h);
+    const int k = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (k >= K) return;
+    for (int i = blockIdx.y; i < M; i += gridDim.y) {
+        const float *a = A + (int64_t)i * lda + k;
+        float v[4];
+        if (VEC_A && k + 3 < K) {
+            const float4 q = *reinterpret_cast<const float4 *>(a);
+            v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = k + j < K ? a[j] : 0.f;
+        }
+        float h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            h[j] = to_tf32_rna(v[j]);
+            l[j] = to_tf32_rna(v[j] - h[j]);
+        }
+        *reinterpret_cast<float4 *>(hi + (int64_t)i * ldo + k) = make_float4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<float4 *>(lo + (int64_t)i * ldo + k) = make_float4(l[0], l[1], l[2], l[3]);
     }
 }
 
@@ -84,33 +101,39 @@ __global__ void __launch_bounds__(256) split_transpose_tf32_kernel(int K, int N,
 
 // ---------------------------------------------------------------- tensor-core product
 
-template <int BN_, int STAGES_>
+// BK = 32 stores operand rows of 128 bytes (128-byte swizzle); BK = 16 rows of
+// 64 bytes (64-byte swizzle), which halves a stage so more stages fit.
+template <int BN_, int BK_, int STAGES_>
 struct Tf32x3Tile {
-    static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_;
+    static constexpr int BM = 128, BN = BN_, BK = BK_, STAGES = STAGES_;
     static constexpr int THREADS = 128;           // 4 warps: copies (warp 0), MMA (warp 1), all 4 drain TMEM
     static constexpr int UMMA_K = 8;              // TF32 elements per tcgen05.mma
-    static constexpr int A_BYTES = BM * BK * 4;   // one operand box: 128 rows of 128 bytes
-    static constexpr int B_BYTES = BN * BK * 4;
+    static constexpr int ROW = BK * 4;            // bytes per operand row = swizzle span
+    static constexpr int A_BYTES = BM * ROW;      // one operand box: 128 rows
+    static constexpr int B_BYTES = BN * ROW;
     static constexpr int STAGE = 2 * A_BYTES + 2 * B_BYTES;  // A_hi, A_lo, B_hi^T, B_lo^T
     static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 /* alignment */ + 256 /* barriers, flags */;
     static constexpr int TMEM_COLS = BN;          // FP32 accumulator: 128 lanes x BN columns
-    static constexpr int SBO = 8 * 128;           // bytes between 8-row groups of a 128-byte-swizzled box
+    static constexpr int SBO = 8 * ROW;           // bytes between 8-row groups of a swizzled box
+    static constexpr uint32_t LAYOUT = ROW == 128 ? 2u : 4u;  // descriptor swizzle mode: 128-byte or 64-byte
     // instruction descriptor: D = F32 (bits 4-5 = 1), A = B = TF32 (bits 7-9, 10-12 = 2),
     // both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
     static constexpr uint32_t IDESC =
         (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+    static_assert(BK == 32 || BK == 16, "operand rows of 128 or 64 bytes");
     static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation: power of two >= 32");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-// Shared-memory matrix descriptor for a K-major operand stored in 128-byte
-// swizzled rows (the layout the TMA's 128-byte swizzle writes): start address,
-// leading-byte offset (unused for this layout, set to 1), stride-byte offset
-// between 8-row groups, descriptor version 1 (bit 46), swizzle mode 2.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t sbo) {
+// Shared-memory matrix descriptor for a K-major operand stored in swizzled
+// rows (the layout the TMA's 128- or 64-byte swizzle writes): start address,
+// leading-byte offset (unused for these layouts, set to 1), stride-byte offset
+// between 8-row groups, descriptor version 1 (bit 46), swizzle mode (bits
+// 61-63: 2 = 128-byte, 4 = 64-byte).
+__device__ __forceinline__ uint64_t umma_desc_swizzled(uint32_t saddr, uint32_t sbo, uint32_t layout) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
-           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+           ((uint64_t)1u << 46) | ((uint64_t)layout << 61);
 }
 
 template <class T, bool VEC_C>
@@ -198,8 +221,8 @@ __global__ void __launch_bounds__(T::THREADS, 1)
                 const uint32_t b = p == 1 ? bl : bh;
 #pragma unroll
                 for (int kk = 0; kk < T::BK / T::UMMA_K; ++kk) {
-                    const uint64_t da = umma_desc_sw128(a + kk * T::UMMA_K * 4, T::SBO);
-                    const uint64_t db = umma_desc_sw128(b + kk * T::UMMA_K * 4, T::SBO);
+                    const uint64_t da = umma_desc_swizzled(a + kk * T::UMMA_K * 4, T::SBO, T::LAYOUT);
+                    const uint64_t db = umma_desc_swizzled(b + kk * T::UMMA_K * 4, T::SBO, T::LAYOUT);
                     umma_tf32(tmem, da, db, T::IDESC, (kt | p | kk) != 0);
                 }
             }
@@ -240,7 +263,9 @@ __global__ void __launch_bounds__(T::THREADS, 1)
     if (warp == 0) tmem_dealloc(tmem, T::TMEM_COLS);
 }
 
-// Shipped configuration: 128 x 256 output tiles, two 96 KiB stages.
-using Tf32x3MainTile = Tf32x3Tile<256, 2>;
+// Shipped configuration: 128 x 256 output tiles, 16-deep k-steps with 64-byte
+// swizzled rows, four 48 KiB stages -- chosen by measurement at 8192^3 among
+// BN in {64, 128, 256}, BK in {16, 32} and 2 to 6 stages.
+using Tf32x3MainTile = Tf32x3Tile<256, 16, 4>;
 
 }  // namespace sgemm
