@@ -277,7 +277,8 @@ def time_steps(step, steps, stream, dev):
 def kernel_name(M, N, K):
     """The kernel sgemm_f32 launches for a contiguous M x K by K x N product."""
     if K > 0 and K % 4 == 0 and N % 4 == 0:
-        return "sgemm_ffma_tma_kernel (256x128x32 TMA-fed tile, 3 stages, 16x8 per thread)"
+        return ("sgemm_ffma_tma_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as fma.rn.f32x2 "
+                "column pairs, 2 CTAs/SM)")
     return "sgemm_ffma_kernel (128x128x16 cp.async tile, 4 stages, 8x8 per thread)"
 
 

@@ -18,12 +18,15 @@
 //    that read different rows in one 16-byte load always hit eight different
 //    bank groups ("Memory hierarchy -- visual walkthrough", Step 6: padding or
 //    an equivalent permutation spreads a column across the banks).
-//  * Each thread keeps a TM x TN block of C (16 x 8 in the shipped
+//  * Each thread keeps a TM x TN block of C (8 x 16 in the shipped
 //    configuration): per group of four k it loads four k-values for each of
 //    its TM rows of A (TM loads of 16 bytes), and per k a TN-wide row vector of
-//    B (TN/4 loads of 16 bytes), then does TM * TN FFMAs -- for 16 x 8, 24
-//    shared loads per 512 multiply-adds ("SGEMM: 2D Register Tiling
-//    Visualizer", 'Why this matters on real GPUs').
+//    B (TN/4 loads of 16 bytes), then does TM * TN multiply-adds -- for 8 x 16,
+//    24 shared loads per 512 multiply-adds ("SGEMM: 2D Register Tiling
+//    Visualizer", 'Why this matters on real GPUs').  The shipped form issues
+//    them as 64 packed two-wide FMAs (fma.rn.f32x2, two round-to-nearest FP32
+//    FMAs each): half the instructions, which leaves the issue slots the
+//    loads need.
 //  * Lane bits are split so that every quarter-warp reads at most two distinct
 //    16-byte chunks of B (broadcast) and at most four of A.
 //  * Every wait on an mbarrier is bounded; on a timeout the CTA leaves the loop
@@ -46,10 +49,17 @@ namespace sgemm {
 // reused across a row of B values), 1 = column-major, 2 = rows in pairs.
 // G_UNROLL: how many of the BK/4 groups of four k are unrolled (code size vs
 // instruction-cache reach).
-template <int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_, int ORDER_, int MIN_BLOCKS_, int G_UNROLL_ = 8>
+// PACKED: accumulate column pairs with the packed instruction fma.rn.f32x2
+// (two round-to-nearest FP32 FMAs per instruction, the same arithmetic as two
+// scalar FFMAs): a row of B gives its pairs directly from the 16-byte loads
+// and the A value is duplicated into both halves; half the FMA instructions
+// leaves issue slots for the loads.
+template <int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_, int ORDER_, int MIN_BLOCKS_, int G_UNROLL_ = 8,
+          bool PACKED_ = false>
 struct TmaTile {
     static constexpr int TM = TM_, TN = TN_, WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
     static constexpr int STAGES = STAGES_, ORDER = ORDER_, MIN_BLOCKS = MIN_BLOCKS_, G_UNROLL = G_UNROLL_;
+    static constexpr bool PACKED = PACKED_;
     static constexpr int WM = 8 * TM, WN = 4 * TN;
     static constexpr int BM = WARPS_M * WM, BN = WARPS_N * WN, BK = 32;
     static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
@@ -63,12 +73,14 @@ struct TmaTile {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
-// The shipped configuration: 256 x 128 block tile, 8 warps of 128 x 32, 16 x 8
-// outputs per thread in row-major FFMA order, 3 stages, k-groups unrolled by
-// two -- chosen by measurement at M = N = K = 8192 among tile shapes (8x8,
-// 8x12, 8x16, 12x8, 16x8 per thread; 128 to 512 threads), FFMA orders, stage
-// counts and unroll depths.
-using TmaMainTile = TmaTile<16, 8, 2, 4, 3, 0, 1, 2>;
+// The shipped configuration: 128 x 128 block tile, 4 warps of 64 x 64, 8 x 16
+// outputs per thread accumulated as column pairs with fma.rn.f32x2 in
+// column-pair-outer order, 3 stages, k-groups unrolled by four, two CTAs per
+// SM.  Chosen by measurement at M = N = K = 8192 among scalar and packed
+// forms, per-thread tiles (8x8 .. 16x16), 128 to 512 threads, FFMA orders,
+// 2 to 4 stages and unroll depths: 82 % of the FP32 peak against 72 % for the
+// best scalar form (16 x 8, row-major order).
+using TmaMainTile = TmaTile<8, 16, 2, 2, 3, 1, 2, 4, true>;
 
 // Error codes written to the device error word.
 enum : int { kDeviceErrNone = 0, kDeviceErrTimeout = 1 };
@@ -141,11 +153,20 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     const int row0 = warp_m * T::WM + lm;          // thread rows: row0 + 8 i, i < TM
     const int col0 = warp_n * T::WN + ln * 4;      // thread cols: col0 + 16 q + (0..3), q < TN / 4
 
-    float acc[T::TM][T::TN];
+    // scalar accumulators, or column pairs for the packed form (one of the two is used)
+    float acc[T::PACKED ? 1 : T::TM][T::PACKED ? 1 : T::TN];
+    uint64_t acc2[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1];
+    if constexpr (T::PACKED) {
 #pragma unroll
-    for (int i = 0; i < T::TM; ++i)
+        for (int i = 0; i < T::TM; ++i)
 #pragma unroll
-        for (int j = 0; j < T::TN; ++j) acc[i][j] = 0.f;
+            for (int j = 0; j < T::TN / 2; ++j) acc2[i][j] = 0ull;
+    } else {
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < T::TN; ++j) acc[i][j] = 0.f;
+    }
 
     int failed_kt = -1;
     for (int kt = 0; kt < KT; ++kt) {
@@ -164,6 +185,35 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const unsigned char *bk = sb + (4 * g + kk) * (T::BN * 4);
+                    if constexpr (T::PACKED) {
+                        uint64_t b2[T::TN / 2];
+#pragma unroll
+                        for (int q = 0; q < T::TN / 4; ++q) {
+                            const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(bk + 64 * q);
+                            b2[2 * q] = v.x;
+                            b2[2 * q + 1] = v.y;
+                        }
+                        if (T::ORDER == 1) {
+                            // column-pair outer: one B pair reused down the TM rows
+                            uint64_t ad[T::TM];
+#pragma unroll
+                            for (int i = 0; i < T::TM; ++i)
+                                ad[i] = f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
+#pragma unroll
+                            for (int j = 0; j < T::TN / 2; ++j)
+#pragma unroll
+                                for (int i = 0; i < T::TM; ++i) f32x2_fma(acc2[i][j], ad[i], b2[j]);
+                        } else {
+                            // row outer: one duplicated A value reused across the row of pairs
+#pragma unroll
+                            for (int i = 0; i < T::TM; ++i) {
+                                const uint64_t ad =
+                                    f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
+#pragma unroll
+                                for (int j = 0; j < T::TN / 2; ++j) f32x2_fma(acc2[i][j], ad, b2[j]);
+                            }
+                        }
+                    } else {
                     float b[T::TN];
 #pragma unroll
                     for (int q = 0; q < T::TN / 4; ++q) {
@@ -196,6 +246,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
                             for (int j = 0; j < T::TN; ++j) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
                     }
+                    }  // scalar form
                 }
             }
         }
@@ -229,7 +280,15 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
         for (int q = 0; q < T::TN / 4; ++q) {
             const int col = n0 + col0 + 16 * q;
-            const float *v = &acc[i][4 * q];
+            float vp[4];
+            if constexpr (T::PACKED) {
+                const float2 lo = f32x2_unpack(acc2[i][2 * q]), hi = f32x2_unpack(acc2[i][2 * q + 1]);
+                vp[0] = lo.x, vp[1] = lo.y, vp[2] = hi.x, vp[3] = hi.y;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) vp[j] = acc[i][4 * q + j];
+            }
+            const float *v = vp;
             if (VEC_C && col + 3 < N) {
                 stg128(crow + col, v[0], v[1], v[2], v[3]);
             } else {

@@ -35,6 +35,24 @@ __device__ __forceinline__ void stg128(float *p, float a, float b, float c, floa
 }
 
 
+// ---------------------------------------------------------------- packed FP32 pairs (sm_100+)
+
+// Two FP32 values in one 64-bit register pair: low half = first value.
+__device__ __forceinline__ uint64_t f32x2_dup(float a) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};\n" : "=l"(r) : "f"(a));
+    return r;
+}
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+// d = a * b + d on both halves, each an IEEE round-to-nearest single-precision FMA.
+__device__ __forceinline__ void f32x2_fma(uint64_t &d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;\n" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // ---------------------------------------------------------------- mbarrier / TMA (sm_90+)
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

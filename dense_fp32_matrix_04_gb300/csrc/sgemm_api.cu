@@ -323,11 +323,11 @@ int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits) {
     if ((int64_t)M * N == 0 || K == 0) return SGEMM_OK;
     DeviceInfo info;
     if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
-    // one TMA tile per SM at a time: split until the (tiles x splits) grid
-    // fills the SMs, keeping at least four 32-deep k-steps per split
+    // MIN_BLOCKS TMA tiles per SM at a time: split until the (tiles x splits)
+    // grid fills the SMs, keeping at least four 32-deep k-steps per split
     const int64_t tiles = (int64_t)((M + TmaTile::BM - 1) / TmaTile::BM) * ((N + TmaTile::BN - 1) / TmaTile::BN);
     const int64_t kt = (K + TmaTile::BK - 1) / TmaTile::BK;
-    int64_t s = info.sms / (tiles > 0 ? tiles : 1);
+    int64_t s = (int64_t)info.sms * TmaTile::MIN_BLOCKS / (tiles > 0 ? tiles : 1);
     if (s > kt / 4) s = kt / 4;
     if (s > kMaxSplits) s = kMaxSplits;
     *splits = (int)(s < 1 ? 1 : s);

@@ -60,9 +60,9 @@ typedef enum {
  * Register-tiled FP32 FFMA kernels with thread-block tiles staged in shared
  * memory through a multi-stage pipeline:
  *   - A and B with 16-byte aligned bases and leading dimensions (multiples of
- *     4 floats), K >= 1: 256 x 128 block tiles copied by the tensor memory
- *     accelerator (TMA) with hardware zero-fill at the edges, 16 x 8 outputs
- *     per thread;
+ *     4 floats), K >= 1: 128 x 128 block tiles copied by the tensor memory
+ *     accelerator (TMA) with hardware zero-fill at the edges, 8 x 16 outputs
+ *     per thread accumulated with packed two-wide FP32 FMAs;
  *   - otherwise: 128 x 128 block tiles copied by cp.async with per-element
  *     masks, 8 x 8 outputs per thread.
  * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
@@ -108,8 +108,8 @@ size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits);
 
 /*
  * A split count for M x N x K on the current device: enough splits for the
- * grid of 256 x 128 output tiles to reach one block per SM, with at least four
- * 32-deep k-steps per split (1 when the tiles already fill the GPU).
+ * grid of 128 x 128 output tiles to reach two blocks per SM, with at least
+ * four 32-deep k-steps per split (1 when the tiles already fill the GPU).
  */
 int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
 
