@@ -70,7 +70,7 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
-    p.add_argument("--path", choices=["ffma", "splitk", "3xtf32"], default="ffma",
+    p.add_argument("--path", choices=["ffma", "splitk", "3xtf32"] + sorted(LADDER), default="ffma",
                    help="ffma: sgemm_f32 (the headline); splitk: sgemm_f32_splitk with the suggested split "
                         "count; 3xtf32: sgemm_f32_3xtf32 (tensor cores). Workspaces are allocated untimed.")
     p.add_argument("--no-variants", action="store_true",
@@ -226,6 +226,9 @@ def recorded_traffic():
 
 # ---------------------------------------------------------------------- arms
 
+LADDER = {"ladder-naive": 0, "ladder-tiled16": 1, "ladder-tiled32": 2, "ladder-tiled32p": 3, "ladder-register": 4}
+
+
 def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
     """One step of the chosen path through the C interface; workspaces are allocated here, untimed."""
     import torch
@@ -238,6 +241,12 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
         def step():
             sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
         return step, (2 if splits > 1 else 1)
+    if path in LADDER:
+        cfg["path"] = path
+
+        def step():
+            sg.sgemm_f32_ladder(LADDER[path], M, N, K, dA, K, dB, N, dC, N, handle)
+        return step, 1
     if path == "3xtf32":
         ws_bytes = sg.sgemm_f32_3xtf32_workspace_size(M, N, K)
         ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
@@ -430,6 +439,8 @@ def run_ours(args):
     roofline["hbm_floor_ms"] = t_hbm * 1e3
     roofline["kernel"] = kernel_name(M, N, K) + (f" + split-K x{cfg['splitk']} with reduction"
                                                  if cfg.get("splitk", 1) > 1 else "")
+    if args.path in LADDER:
+        roofline["kernel"] = f"{args.path} (the pages' kernel ladder)"
     if args.path == "3xtf32":
         tpk, tsrc = tf32_peak_tflops()
         roofline = {"bound": "tensor", "achieved": 3 * flop / per_launch_s / 1e12, "peak": tpk, "unit": "TFLOP/s",

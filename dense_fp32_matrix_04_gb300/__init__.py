@@ -31,6 +31,12 @@ SGEMM_ERR_DEVICE = 4
 SGEMM_ERR_TIMEOUT = 5
 SGEMM_ERR_SCRATCH_LIMIT = 6
 
+LADDER_NAIVE = 0
+LADDER_TILED_16 = 1
+LADDER_TILED_32 = 2
+LADDER_TILED_32_PADDED = 3
+LADDER_REGISTER_2D = 4
+
 #: Every entry point include/sgemm.h declares, with its ctypes signature.
 _SIGNATURES = {
     "sgemm_f32": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -53,6 +59,9 @@ _SIGNATURES = {
     "sgemm_f32_3xtf32_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "sgemm_f32_splitk_suggest": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_int)]),
+    "sgemm_f32_ladder": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "sgemm_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
 }
@@ -202,6 +211,15 @@ def matmul_splitk(A, B, out=None, splits=None, workspace=None, stream=None):
     lda, ldb, ldc = _rows(A, "A"), _rows(B, "B"), _rows(out, "out")
     sgemm_f32_splitk(M, N, K, A, lda, B, ldb, out, ldc, splits, workspace, workspace.numel() * 4, stream)
     return out
+
+
+def sgemm_f32_ladder(level: int, M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int,
+                     stream=None) -> None:
+    """One of the pages' ladder kernels (naive, tiled, register-tiled); see include/sgemm.h."""
+    lib = load()
+    st = lib.sgemm_f32_ladder(int(level), int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C),
+                              int(ldc), _stream(stream))
+    _check(st, "sgemm_f32_ladder")
 
 
 def sgemm_device_status(stream=None) -> int:

@@ -12,6 +12,7 @@
 #include "../../include/sgemm.h"
 #include "ffma_sgemm.cuh"
 #include "ffma_tma_sgemm.cuh"
+#include "ladder.cuh"
 #include "splitk_reduce.cuh"
 #include "tf32x3_tcgen05.cuh"
 
@@ -410,6 +411,39 @@ int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, const float *
     DeviceInfo info;
     if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
     return launch_3xtf32(p, workspace, stream, info);
+}
+
+int sgemm_f32_ladder(int level, int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C,
+                     int ldc, cudaStream_t stream) {
+    const Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    const int st = validate(p);
+    if (st != SGEMM_OK) return st;
+    if (level < SGEMM_LADDER_NAIVE || level > SGEMM_LADDER_REGISTER_2D) return SGEMM_ERR_INVALID_ARG;
+    if ((int64_t)M * N == 0) return SGEMM_OK;
+    const int rows_per_block = level == SGEMM_LADDER_REGISTER_2D ? 64 : (level == SGEMM_LADDER_NAIVE || level == SGEMM_LADDER_TILED_16) ? 16 : 32;
+    if ((M + rows_per_block - 1) / rows_per_block > 65535) return SGEMM_ERR_INVALID_ARG;
+    switch (level) {
+        case SGEMM_LADDER_NAIVE:
+            sgemm::ladder_naive_kernel<<<dim3((N + 15) / 16, (M + 15) / 16), dim3(16, 16), 0, stream>>>(
+                M, N, K, A, lda, B, ldb, C, ldc);
+            break;
+        case SGEMM_LADDER_TILED_16:
+            sgemm::ladder_tiled_kernel<16, 0><<<dim3((N + 15) / 16, (M + 15) / 16), dim3(16, 16), 0, stream>>>(
+                M, N, K, A, lda, B, ldb, C, ldc);
+            break;
+        case SGEMM_LADDER_TILED_32:
+            sgemm::ladder_tiled_kernel<32, 0><<<dim3((N + 31) / 32, (M + 31) / 32), dim3(32, 32), 0, stream>>>(
+                M, N, K, A, lda, B, ldb, C, ldc);
+            break;
+        case SGEMM_LADDER_TILED_32_PADDED:
+            sgemm::ladder_tiled_kernel<32, 1><<<dim3((N + 31) / 32, (M + 31) / 32), dim3(32, 32), 0, stream>>>(
+                M, N, K, A, lda, B, ldb, C, ldc);
+            break;
+        default:
+            sgemm::ladder_register_kernel<64, 64, 8, 4, 4><<<dim3((N + 63) / 64, (M + 63) / 64), 256, 0, stream>>>(
+                M, N, K, A, lda, B, ldb, C, ldc);
+    }
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
 int sgemm_device_status(cudaStream_t stream) {

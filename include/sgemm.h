@@ -180,6 +180,39 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K,
                              int splits, cudaStream_t stream);
 
 /*
+ * The pages' kernel ladder, as GPU kernels: the reference points the tuned
+ * kernels are measured against, and the kernels whose executed global loads
+ * the pages count.  Every level computes C = A * B with the same contract,
+ * shapes, strides, masks and errors as sgemm_f32 (plain loads: any 4-byte
+ * alignment), one FP32 FMA chain per output in increasing k.
+ *   SGEMM_LADDER_NAIVE: one thread per output, operands read straight from
+ *     global memory, 2MNK loads ("Shared Memory Tiling", 'The naive kernel').
+ *   SGEMM_LADDER_TILED_16 / _32: T x T thread blocks staging T x T tiles of A
+ *     and B in shared memory with zero-filled edges, 2MNK/T loads for
+ *     T-divisible shapes ("SGEMM: Shared Memory Tiling Visualizer", the tiled
+ *     kernel); _32_PADDED uses [32][33] tiles ("Shared Memory Tiling",
+ *     'Conflict-free layout').
+ *   SGEMM_LADDER_REGISTER_2D: 64 x 64 x 8 block tiles, 4 x 4 outputs per
+ *     thread from register outer products ("SGEMM: 2D Register Tiling
+ *     Visualizer", the listing).
+ * Row-block counts above 65535 (M > 65535 x 16 / 32 / 64) return
+ * SGEMM_ERR_INVALID_ARG.
+ */
+typedef enum {
+    SGEMM_LADDER_NAIVE = 0,
+    SGEMM_LADDER_TILED_16 = 1,
+    SGEMM_LADDER_TILED_32 = 2,
+    SGEMM_LADDER_TILED_32_PADDED = 3,
+    SGEMM_LADDER_REGISTER_2D = 4
+} sgemm_ladder_level;
+
+int sgemm_f32_ladder(int level, int M, int N, int K,
+                     const float *A, int lda,
+                     const float *B, int ldb,
+                     float *C, int ldc,
+                     cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears this device's error word, which
  * kernels set when a bounded wait runs out.  SGEMM_OK if no kernel gave up
  * since the last call, SGEMM_ERR_TIMEOUT if one did, SGEMM_ERR_DEVICE if a

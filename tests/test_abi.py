@@ -135,6 +135,28 @@ def test_build_targets_sm_103a_only():
     assert not re.search(r"[1-9]\d* bytes spill stores", log)
 
 
+def _smem_of(log, kernel_regex):
+    """Static shared memory ptxas reports for the first kernel whose mangled name matches."""
+    lines = log.splitlines()
+    for i, line in enumerate(lines):
+        if "Compiling entry function" in line and re.search(kernel_regex, line):
+            for follow in lines[i + 1:i + 4]:
+                m = re.search(r"(\d+) bytes smem", follow)
+                if m:
+                    return int(m.group(1))
+    raise AssertionError(f"no ptxas report for {kernel_regex}")
+
+
+def test_ladder_tiles_reproduce_the_pages_shared_memory_table():
+    # "Shared Memory Tiling", 'Choosing a tile size': 2 x 16 x 16 x 4 = 2048 bytes
+    # (T = 16, unpadded) and 2 x 32 x 33 x 4 = 8448 bytes (T = 32, padded), the
+    # latter quoted from an -Xptxas -v report -- here read from this build's
+    log = open(os.path.join(build.BUILD_DIR, "ptxas.log")).read()
+    assert _smem_of(log, r"ladder_tiled_kernelILi16ELi0E") == 2048
+    assert _smem_of(log, r"ladder_tiled_kernelILi32ELi1E") == 8448
+    assert _smem_of(log, r"ladder_tiled_kernelILi32ELi0E") == 8192
+
+
 def test_product_package_never_imports_the_oracle():
     pkg = os.path.dirname(sg.__file__)
     for root, _, files in os.walk(pkg):
