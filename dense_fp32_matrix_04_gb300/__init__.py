@@ -31,6 +31,11 @@ SGEMM_ERR_DEVICE = 4
 SGEMM_ERR_TIMEOUT = 5
 SGEMM_ERR_SCRATCH_LIMIT = 6
 
+OP_N = 0
+OP_T = 1
+ALGO_FFMA = 0
+ALGO_3XTF32 = 1
+
 LADDER_NAIVE = 0
 LADDER_TILED_16 = 1
 LADDER_TILED_32 = 2
@@ -62,6 +67,12 @@ _SIGNATURES = {
     "sgemm_f32_ladder": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
+    "sgemm_gemm": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                  ctypes.c_void_p]),
+    "sgemm_gemm_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int]),
     "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "sgemm_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
 }
@@ -220,6 +231,20 @@ def sgemm_f32_ladder(level: int, M: int, N: int, K: int, A, lda: int, B, ldb: in
     st = lib.sgemm_f32_ladder(int(level), int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C),
                               int(ldc), _stream(stream))
     _check(st, "sgemm_f32_ladder")
+
+
+def sgemm_gemm(algo: int, transa: int, transb: int, M: int, N: int, K: int, alpha: float, A, lda: int, B,
+               ldb: int, beta: float, C, ldc: int, workspace=None, workspace_bytes: int = 0, stream=None) -> None:
+    """C = alpha op(A) op(B) + beta C (row-major, BLAS-style); see include/sgemm.h."""
+    lib = load()
+    st = lib.sgemm_gemm(int(algo), int(transa), int(transb), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda),
+                        _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc), _ptr(workspace), int(workspace_bytes),
+                        _stream(stream))
+    _check(st, "sgemm_gemm")
+
+
+def sgemm_gemm_workspace_size(algo: int, transa: int, transb: int, M: int, N: int, K: int) -> int:
+    return int(load().sgemm_gemm_workspace_size(int(algo), int(transa), int(transb), int(M), int(N), int(K)))
 
 
 def sgemm_device_status(stream=None) -> int:

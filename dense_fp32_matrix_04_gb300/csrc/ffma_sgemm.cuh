@@ -33,6 +33,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "tile_map.cuh"
 
@@ -74,8 +75,9 @@ struct FfmaTile {
 
 template <class T, bool VEC_B, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
-    sgemm_ffma_kernel(int M, int N, int K, const float *__restrict__ A, int lda, const float *__restrict__ B,
-                      int ldb, float *__restrict__ C, int ldc, float *__restrict__ partials, int ldp) {
+    sgemm_ffma_kernel(int M, int N, int K, float alpha, const float *__restrict__ A, int lda,
+                      const float *__restrict__ B, int ldb, float beta, float *__restrict__ C, int ldc,
+                      float *__restrict__ partials, int ldp) {
     extern __shared__ __align__(16) float smem[];
     float *sA = smem;                          // [STAGES][BK][A_LD]
     float *sB = smem + T::STAGES * T::A_STAGE;  // [STAGES][BK][B_LD]
@@ -246,14 +248,9 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
             for (int qn = 0; qn < 2; ++qn) {
                 const int col = n0 + frag_b + qn * 16;
-                const float *v = &acc[qm * 4 + i][qn * 4];
-                if (VEC_C && col + 3 < N) {
-                    stg128(crow + col, v[0], v[1], v[2], v[3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (col + j < N) crow[col + j] = v[j];
-                }
+                const float v[4] = {acc[qm * 4 + i][qn * 4], acc[qm * 4 + i][qn * 4 + 1], acc[qm * 4 + i][qn * 4 + 2],
+                                    acc[qm * 4 + i][qn * 4 + 3]};
+                store_quad<VEC_C>(crow, col, N, v, alpha, beta);
             }
         }
     }

@@ -37,6 +37,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "tile_map.cuh"
 
@@ -92,8 +93,9 @@ enum : int { kDebugSkipCopies = 1 };
 template <class T, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
-                          int N, int K, float *__restrict__ C, int ldc, float *__restrict__ partials, int ldp,
-                          int *__restrict__ err_word, unsigned long long wait_limit_ns, int debug) {
+                          int N, int K, float alpha, float beta, float *__restrict__ C, int ldc,
+                          float *__restrict__ partials, int ldp, int *__restrict__ err_word,
+                          unsigned long long wait_limit_ns, int debug) {
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern
     const uint32_t raw = smem_addr(smem_raw);
@@ -271,7 +273,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         return;
     }
 
-    // epilogue: rows row0 + 8 i, 16-byte column quads at col0 + 16 q
+    // epilogue: rows row0 + 8 i, 16-byte column quads at col0 + 16 q;
+    // C = alpha * acc + beta * C (partial slabs are written with alpha = 1, beta = 0)
 #pragma unroll
     for (int i = 0; i < T::TM; ++i) {
         const int row = m0 + row0 + 8 * i;
@@ -288,14 +291,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) vp[j] = acc[i][4 * q + j];
             }
-            const float *v = vp;
-            if (VEC_C && col + 3 < N) {
-                stg128(crow + col, v[0], v[1], v[2], v[3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (col + j < N) crow[col + j] = v[j];
-            }
+            store_quad<VEC_C>(crow, col, N, vp, alpha, beta);
         }
     }
 }

@@ -110,6 +110,9 @@ bool smem_attr_once(std::atomic<int> &done, Kernel kernel, int bytes) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// C = alpha * op(A) op(B) + beta * C.  The product kernels take A as M x K and
+// B as K x N row-major; transa / transb mean A is stored K x M and B N x K
+// (only the 3xTF32 split pass reads those orientations directly).
 struct Problem {
     int M, N, K;
     const float *A;
@@ -118,6 +121,8 @@ struct Problem {
     int ldb;
     float *C;
     int ldc;
+    float alpha = 1.f, beta = 0.f;
+    bool transa = false, transb = false;
 };
 
 // The TMA kernel needs 16-byte aligned bases and row strides and K >= 1.
@@ -148,6 +153,8 @@ bool cp_attr(int dev) {
 int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
                    const DeviceInfo &info) {
     const bool vc = splits > 1 || (aligned16(p.C) && p.ldc % 4 == 0);
+    // partial slabs hold the raw products; alpha and beta act in the reduction
+    const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
     if (use_tma(p)) {
         using T = TmaTile;
         alignas(64) CUtensorMap ta, tb;
@@ -157,7 +164,7 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
         if (!(vc ? tma_attr<T, true>(info.dev) : tma_attr<T, false>(info.dev))) return SGEMM_ERR_LAUNCH;
         auto kernel = vc ? sgemm::sgemm_ffma_tma_kernel<T, true> : sgemm::sgemm_ffma_tma_kernel<T, false>;
         const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
-        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, p.C, p.ldc, partials, ldp,
+        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc, partials, ldp,
                                                             info.err_word, g_wait_limit_ns.load(),
                                                             g_debug_flags.load());
     } else {
@@ -169,8 +176,8 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
         auto kernel = vb ? (vc ? sgemm::sgemm_ffma_kernel<T, true, true> : sgemm::sgemm_ffma_kernel<T, true, false>)
                          : (vc ? sgemm::sgemm_ffma_kernel<T, false, true> : sgemm::sgemm_ffma_kernel<T, false, false>);
         const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
-        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc, partials,
-                                                            ldp);
+        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p.M, p.N, p.K, alpha, p.A, p.lda, p.B, p.ldb, beta, p.C,
+                                                            p.ldc, partials, ldp);
     }
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
@@ -181,9 +188,11 @@ int launch_reduce(const Problem &p, int splits, const float *partials, int ldp, 
     const int64_t want = (quads + 255) / 256;
     const int blocks = (int)(want < (int64_t)info.sms * 8 ? want : (int64_t)info.sms * 8);
     if (aligned16(p.C) && p.ldc % 4 == 0)
-        sgemm::splitk_reduce_kernel<true><<<blocks, 256, 0, stream>>>(p.M, p.N, splits, partials, ldp, p.C, p.ldc);
+        sgemm::splitk_reduce_kernel<true>
+            <<<blocks, 256, 0, stream>>>(p.M, p.N, splits, partials, ldp, p.alpha, p.beta, p.C, p.ldc);
     else
-        sgemm::splitk_reduce_kernel<false><<<blocks, 256, 0, stream>>>(p.M, p.N, splits, partials, ldp, p.C, p.ldc);
+        sgemm::splitk_reduce_kernel<false>
+            <<<blocks, 256, 0, stream>>>(p.M, p.N, splits, partials, ldp, p.alpha, p.beta, p.C, p.ldc);
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
@@ -219,6 +228,18 @@ int validate(const Problem &p) {
 
 int ld_partials(int N) { return ((N + 3) / 4) * 4; }
 
+int64_t ld4(int n) { return ((int64_t)n + 3) / 4 * 4; }
+
+// Workspace of the FFMA form of sgemm_gemm: row-major copies of the operands
+// given transposed (A^T -> M x K, B^T -> K x N, rows padded to 4 floats).
+size_t gemm_ffma_workspace(int transa, int transb, int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    size_t b = 0;
+    if (transa) b += (size_t)M * (size_t)ld4(K) * sizeof(float);
+    if (transb) b += (size_t)K * (size_t)ld4(N) * sizeof(float);
+    return b;
+}
+
 size_t partials_bytes(int M, int N, int splits) {
     if (splits <= 1 || M <= 0 || N <= 0) return 0;
     return (size_t)splits * (size_t)M * (size_t)ld_partials(N) * sizeof(float);
@@ -239,14 +260,23 @@ int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const Device
     const int64_t kp = x3_kpad(p.K);
     float *ah = ws, *al = ws + (int64_t)p.M * kp;
     float *bh = al + (int64_t)p.M * kp, *bl = bh + (int64_t)p.N * kp;
-    const int quads = (p.K + 3) / 4;
-    const dim3 rgrid((unsigned)((quads + 255) / 256), (unsigned)(p.M < 65535 ? p.M : 65535));
-    if (aligned16(p.A) && p.lda % 4 == 0)
-        sgemm::split_rows_tf32_kernel<true><<<rgrid, 256, 0, stream>>>(p.M, p.K, p.A, p.lda, ah, al, (int)kp);
-    else
-        sgemm::split_rows_tf32_kernel<false><<<rgrid, 256, 0, stream>>>(p.M, p.K, p.A, p.lda, ah, al, (int)kp);
-    const dim3 tgrid((unsigned)((p.N + 31) / 32), (unsigned)((p.K + 31) / 32));
-    sgemm::split_transpose_tf32_kernel<<<tgrid, 256, 0, stream>>>(p.K, p.N, p.B, p.ldb, bh, bl, (int)kp);
+    // A_hi, A_lo are M x K rows and B_hi, B_lo are N x K rows: a row split of an
+    // operand already stored that way, a transposing split otherwise
+    auto split_rows = [&](int rows, const float *src, int ld, float *hi, float *lo) {
+        const dim3 grid((unsigned)(((p.K + 3) / 4 + 255) / 256), (unsigned)(rows < 65535 ? rows : 65535));
+        if (aligned16(src) && ld % 4 == 0)
+            sgemm::split_rows_tf32_kernel<true><<<grid, 256, 0, stream>>>(rows, p.K, src, ld, hi, lo, (int)kp);
+        else
+            sgemm::split_rows_tf32_kernel<false><<<grid, 256, 0, stream>>>(rows, p.K, src, ld, hi, lo, (int)kp);
+    };
+    auto split_transposed = [&](int cols, const float *src, int ld, float *hi, float *lo) {
+        const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((p.K + 31) / 32));
+        sgemm::split_transpose_tf32_kernel<<<grid, 256, 0, stream>>>(p.K, cols, src, ld, hi, lo, (int)kp);
+    };
+    if (p.transa) split_transposed(p.M, p.A, p.lda, ah, al);  // A stored K x M
+    else split_rows(p.M, p.A, p.lda, ah, al);
+    if (p.transb) split_rows(p.N, p.B, p.ldb, bh, bl);        // B stored N x K
+    else split_transposed(p.N, p.B, p.ldb, bh, bl);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     alignas(64) CUtensorMap tah, tal, tbh, tbl;
     const CUtensorMapSwizzle sw = T::ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -262,7 +292,7 @@ int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const Device
         return SGEMM_ERR_LAUNCH;
     auto kernel = vc ? sgemm::sgemm_3xtf32_kernel<T, true> : sgemm::sgemm_3xtf32_kernel<T, false>;
     const unsigned tiles = (unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN));
-    kernel<<<tiles, T::THREADS, T::SMEM_BYTES, stream>>>(tah, tal, tbh, tbl, p.M, p.N, p.K, p.C, p.ldc,
+    kernel<<<tiles, T::THREADS, T::SMEM_BYTES, stream>>>(tah, tal, tbh, tbl, p.M, p.N, p.K, p.alpha, p.beta, p.C, p.ldc,
                                                          info.err_word, g_wait_limit_ns.load(),
                                                          g_debug_flags.load());
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
@@ -444,6 +474,82 @@ int sgemm_f32_ladder(int level, int M, int N, int K, const float *A, int lda, co
                 M, N, K, A, lda, B, ldb, C, ldc);
     }
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+size_t sgemm_gemm_workspace_size(int algo, int transa, int transb, int M, int N, int K) {
+    if (algo == SGEMM_ALGO_3XTF32) return x3_workspace_bytes(M, N, K);
+    return gemm_ffma_workspace(transa, transb, M, N, K);
+}
+
+int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alpha, const float *A, int lda,
+               const float *B, int ldb, float beta, float *C, int ldc, float *workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+    if ((algo != SGEMM_ALGO_FFMA && algo != SGEMM_ALGO_3XTF32) || (transa != SGEMM_OP_N && transa != SGEMM_OP_T) ||
+        (transb != SGEMM_OP_N && transb != SGEMM_OP_T))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    // stored shapes of A and B
+    const int a_rows = transa ? K : M, a_cols = transa ? M : K;
+    const int b_rows = transb ? N : K, b_cols = transb ? K : N;
+    if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1) || ldc < (N > 1 ? N : 1))
+        return SGEMM_ERR_INVALID_ARG;
+    const bool a_nonempty = (int64_t)M * K > 0, b_nonempty = (int64_t)K * N > 0, c_nonempty = (int64_t)M * N > 0;
+    if ((a_nonempty && !A) || (b_nonempty && !B) || (c_nonempty && !C)) return SGEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 3u)
+        return SGEMM_ERR_INVALID_ARG;
+    if (!c_nonempty) return SGEMM_OK;
+    const int64_t tiles = (int64_t)((M + CpTile::BM - 1) / CpTile::BM) * ((N + CpTile::BN - 1) / CpTile::BN);
+    if (tiles > 0x7fffffff || K > 65535 * 32 || (transb && N > 65535 * 32)) return SGEMM_ERR_INVALID_ARG;
+    uintptr_t c0, c1, a0, a1, b0, b1;
+    span(C, M, N, ldc, c0, c1);
+    span(A, a_rows, a_cols, lda, a0, a1);
+    span(B, b_rows, b_cols, ldb, b0, b1);
+    if ((a_nonempty && overlap(c0, c1, a0, a1)) || (b_nonempty && overlap(c0, c1, b0, b1))) return SGEMM_ERR_ALIAS;
+
+    DeviceInfo info;
+    if (alpha == 0.f || K == 0) {
+        // nothing to multiply: C = beta * C (A and B are not read)
+        if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+        const int64_t want = ((int64_t)M * N + 255) / 256;
+        const int blocks = (int)(want < (int64_t)info.sms * 8 ? want : (int64_t)info.sms * 8);
+        sgemm::scale_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
+        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
+    const size_t need = sgemm_gemm_workspace_size(algo, transa, transb, M, N, K);
+    if (need > 0) {
+        if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
+        const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + need;
+        if (overlap(w0, w1, c0, c1) || (a_nonempty && overlap(w0, w1, a0, a1)) ||
+            (b_nonempty && overlap(w0, w1, b0, b1)))
+            return SGEMM_ERR_ALIAS;
+    }
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+
+    Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    p.alpha = alpha;
+    p.beta = beta;
+    if (algo == SGEMM_ALGO_3XTF32) {
+        p.transa = transa == SGEMM_OP_T;
+        p.transb = transb == SGEMM_OP_T;
+        return launch_3xtf32(p, workspace, stream, info);
+    }
+    // FFMA: transposed operands are first copied row-major into the workspace
+    float *w = workspace;
+    if (transa) {
+        const int ld = (int)ld4(K);
+        sgemm::transpose_kernel<<<dim3((M + 31) / 32, (K + 31) / 32), 256, 0, stream>>>(K, M, A, lda, w, ld);
+        p.A = w;
+        p.lda = ld;
+        w += (int64_t)M * ld;
+    }
+    if (transb) {
+        const int ld = (int)ld4(N);
+        sgemm::transpose_kernel<<<dim3((K + 31) / 32, (N + 31) / 32), 256, 0, stream>>>(N, K, B, ldb, w, ld);
+        p.B = w;
+        p.ldb = ld;
+    }
+    if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    return launch_product(p, 1, nullptr, 0, stream, info);
 }
 
 int sgemm_device_status(cudaStream_t stream) {

@@ -1,5 +1,6 @@
-// Split-K reduction: C = sum over s of the partial products P[s], in increasing
-// s (a fixed order, so the result is the same on every run).
+// Split-K reduction: C = alpha * (sum over s of the partial products P[s]) +
+// beta * C, the sum in increasing s (a fixed order, so the result is the same
+// on every run).
 //
 // P holds S slabs of M rows with leading dimension ldp (a multiple of 4, 16-byte
 // aligned base), written by the split-K product kernels.  Memory-bound: it
@@ -10,11 +11,13 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
+
 namespace sgemm {
 
 template <bool VEC_C>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(int M, int N, int S, const float *__restrict__ P, int ldp,
-                                                            float *__restrict__ C, int ldc) {
+                                                            float alpha, float beta, float *__restrict__ C, int ldc) {
     const int64_t quads = (N + 3) / 4;
     const int64_t total = (int64_t)M * quads;
     const int64_t slab = (int64_t)M * ldp;
@@ -30,15 +33,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(int M, int N, int S,
             acc.z += v.z;
             acc.w += v.w;
         }
-        float *c = C + i * ldc + j;
-        if (VEC_C && j + 3 < N) {
-            *reinterpret_cast<float4 *>(c) = acc;
-        } else {
-            const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-                if (j + jj < N) c[jj] = v[jj];
-        }
+        const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+        store_quad<VEC_C>(C + i * ldc, j, N, v, alpha, beta);
     }
 }
 

@@ -30,12 +30,17 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "tile_map.cuh"
 
 namespace sgemm {
 
 // ---------------------------------------------------------------- operand split (memory-bound)
+
+// (The split kernels take the operand in either stored orientation: A^T stored
+// K x M is split with the transposing kernel, B^T stored N x K with the row
+// kernel, so transposed operands cost no extra pass.)
 
 // hi[i][k], lo[i][k] (leading dimension ldo, a multiple of 4, 16-byte aligned
 // rows) from the M x K matrix A.  Each thread splits a quad of 4 columns: one
@@ -140,8 +145,8 @@ template <class T, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                         const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M,
-                        int N, int K, float *__restrict__ C, int ldc, int *__restrict__ err_word,
-                        unsigned long long wait_limit_ns, int debug) {
+                        int N, int K, float alpha, float beta, float *__restrict__ C, int ldc,
+                        int *__restrict__ err_word, unsigned long long wait_limit_ns, int debug) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -244,14 +249,10 @@ __global__ void __launch_bounds__(T::THREADS, 1)
             float v[32];
             tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
             if (row < M) {
-                const int col = n0 + c0;
-                if (VEC_C && col + 31 < N) {
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) stg128(crow + col + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (col + j < N) crow[col + j] = v[j];
+                for (int j = 0; j < 32; j += 4) {
+                    const float q[4] = {v[j], v[j + 1], v[j + 2], v[j + 3]};
+                    store_quad<VEC_C>(crow, n0 + c0 + j, N, q, alpha, beta);
                 }
             }
         }

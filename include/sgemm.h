@@ -180,6 +180,41 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K,
                              int splits, cudaStream_t stream);
 
 /*
+ * General form: C = alpha * op(A) op(B) + beta * C, BLAS-style, row-major.
+ * The pages' product is the case alpha = 1, beta = 0, no transposes; the
+ * rest is the usual superset (the pages use none of it).
+ *   transa: SGEMM_OP_N -- A is M x K (lda >= K); SGEMM_OP_T -- A is stored
+ *           K x M (lda >= M) and op(A) = A^T.
+ *   transb: SGEMM_OP_N -- B is K x N (ldb >= N); SGEMM_OP_T -- B is stored
+ *           N x K (ldb >= K) and op(B) = B^T.
+ *   beta == 0: C is not read (NaN in C does not propagate).
+ *   alpha == 0 or K == 0: A and B are not read; C = beta * C.
+ *   algo: SGEMM_ALGO_FFMA -- the FP32 FFMA kernels of sgemm_f32; transposed
+ *           operands are first copied row-major into the workspace (one
+ *           memory-bound pass each).
+ *         SGEMM_ALGO_3XTF32 -- the tensor-core path of sgemm_f32_3xtf32; its
+ *           operand split reads either orientation directly.
+ *   workspace: at least sgemm_gemm_workspace_size(...) bytes (0 for FFMA
+ *           without transposes), caller-owned device memory, 16-byte aligned,
+ *           not overlapping A, B or C.
+ * Accuracy: |C - C_exact| <= 2 (K + 2) 2^-24 (|alpha| sum_k |a||b| + |beta||c|).
+ * K <= 2,097,120 (and N <= 2,097,120 when B is transposed); other errors as
+ * for sgemm_f32_3xtf32.
+ */
+typedef enum { SGEMM_OP_N = 0, SGEMM_OP_T = 1 } sgemm_op;
+typedef enum { SGEMM_ALGO_FFMA = 0, SGEMM_ALGO_3XTF32 = 1 } sgemm_algo;
+
+int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K,
+               float alpha, const float *A, int lda,
+               const float *B, int ldb,
+               float beta, float *C, int ldc,
+               float *workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/* Workspace bytes sgemm_gemm needs for this algorithm and operand orientation. */
+size_t sgemm_gemm_workspace_size(int algo, int transa, int transb, int M, int N, int K);
+
+/*
  * The pages' kernel ladder, as GPU kernels: the reference points the tuned
  * kernels are measured against, and the kernels whose executed global loads
  * the pages count.  Every level computes C = A * B with the same contract,

@@ -121,3 +121,31 @@ def gemm_entries(A: np.ndarray, B: np.ndarray, rows, cols):
             r.size, r.ctypes.data_as(_lp), c.ctypes.data_as(_lp),
             out_c.ctypes.data_as(_dp), out_s.ctypes.data_as(_dp))
     return out_c, out_s
+
+
+def op(X: np.ndarray, trans: bool) -> np.ndarray:
+    """op(X) = X or its transpose (a view, no copy)."""
+    return X.T if trans else X
+
+
+def gemm_general_f64(transa: bool, transb: bool, alpha: float, A: np.ndarray, B: np.ndarray, beta: float,
+                     C0: np.ndarray):
+    """``alpha * op(A) op(B) + beta * C0`` in FP64 and its error scale.
+
+    The product term is the oracle's FP64 dot product of rows of op(A) with
+    columns of op(B) (the same definition as ``gemm_f64``, on transposed
+    operands where asked); alpha and beta are applied once per element in
+    FP64.  When beta == 0, C0 is not read (its NaNs do not propagate).
+    Returns ``(C64, S, T)`` with S = sum |a||b| of the product and
+    T = |beta| |C0| (0 where beta == 0).
+    """
+    opA = np.ascontiguousarray(op(np.asarray(A, np.float32), transa))
+    opB = np.ascontiguousarray(op(np.asarray(B, np.float32), transb))
+    P, S = gemm_f64(opA, opB)
+    C64 = float(alpha) * P
+    T = np.zeros_like(C64)
+    if beta != 0.0:
+        C0d = np.asarray(C0, dtype=np.float64)
+        C64 = C64 + float(beta) * C0d
+        T = abs(float(beta)) * np.abs(C0d)
+    return C64, S, T

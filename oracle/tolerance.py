@@ -40,3 +40,20 @@ def max_error_ratio(C, C64, S, K) -> float:
 
 def within(C, C64, S, K) -> bool:
     return max_error_ratio(C, C64, S, K) <= 1.0
+
+
+def bound_general(S, T, K, alpha):
+    """Bound for C = alpha * op(A) op(B) + beta * C0 computed in FP32:
+    the product's 2 K u |alpha| S, plus two more roundings (the scaling by
+    alpha and the final addition) of each term: 2 (K + 2) u (|alpha| S + T)."""
+    return 2.0 * (K + 2) * U32 * (abs(float(alpha)) * np.asarray(S, np.float64) + np.asarray(T, np.float64))
+
+
+def max_error_ratio_general(C, C64, S, T, K, alpha) -> float:
+    C = np.asarray(C, dtype=np.float64)
+    err = np.abs(C - np.asarray(C64, dtype=np.float64))
+    b = bound_general(S, T, K, alpha)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(b > 0, err / np.where(b > 0, b, 1.0), np.where(err > 0, np.inf, 0.0))
+    r = np.where(np.isfinite(C), r, np.inf)
+    return float(r.max()) if r.size else 0.0

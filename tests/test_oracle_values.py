@@ -186,3 +186,36 @@ def test_pins_catch_planted_mistakes(mistake):
         flat = buf.reshape(-1)
         bad, _ = ref_gemm.gemm_f64(np.lib.stride_tricks.as_strided(flat, (6, 9), (9 * 4, 4)), B)
     assert not exact_pin(bad, A, B)
+
+
+# ---------------------------------------------------------------- the general form alpha op(A) op(B) + beta C
+
+def test_general_form_pins():
+    """alpha/beta and transposes: exact small-integer cases checked against
+    brute force written independently of the oracle."""
+    A = gen.matrix(90, gen.STREAM_A_INT, 9, 6, "int")      # stored K x M: op(A) = A^T is 6 x 9
+    B = gen.matrix(90, gen.STREAM_B_INT, 7, 9, "int")      # stored N x K: op(B) = B^T is 9 x 7
+    C0 = gen.matrix(91, gen.STREAM_A_INT, 6, 7, "int")
+    C64, S, T = ref_gemm.gemm_general_f64(True, True, 2.0, A, B, -3.0, C0)
+    want = np.array([[2 * sum(int(A[k, i]) * int(B[j, k]) for k in range(9)) - 3 * int(C0[i, j])
+                      for j in range(7)] for i in range(6)], dtype=np.float64)
+    assert np.array_equal(C64, want)
+    assert np.array_equal(T, 3.0 * np.abs(C0))
+    # beta = 0 never reads C0 (NaN in C0 must not appear)
+    nan_c = np.full((6, 7), np.nan, np.float32)
+    C64b, _, Tb = ref_gemm.gemm_general_f64(True, True, 1.0, A, B, 0.0, nan_c)
+    assert np.isfinite(C64b).all() and np.all(Tb == 0)
+    # no transposes, alpha = 1, beta = 0 is the plain product
+    A2, B2 = gen.operands(5, 4, 3, seed=92, integer_copy=True)
+    assert np.array_equal(ref_gemm.gemm_general_f64(False, False, 1.0, A2, B2, 0.0, None)[0],
+                          ref_gemm.gemm_f64(A2, B2)[0])
+
+
+def test_general_tolerance_accepts_fp32_and_rejects_a_wrong_beta():
+    A, B = gen.operands(6, 6, 9, seed=0)
+    C0 = gen.matrix(93, gen.STREAM_A, 6, 6)
+    C64, S, T = ref_gemm.gemm_general_f64(False, False, 0.5, A, B, 2.0, C0)
+    C32 = (np.float32(0.5) * fp32_sequential(A, B) + np.float32(2.0) * C0).astype(np.float32)
+    assert tolerance.max_error_ratio_general(C32, C64, S, T, 9, 0.5) <= 1.0
+    wrong = (np.float32(0.5) * fp32_sequential(A, B) + np.float32(1.0) * C0).astype(np.float32)
+    assert tolerance.max_error_ratio_general(wrong, C64, S, T, 9, 0.5) > 1.0
