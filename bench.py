@@ -480,16 +480,26 @@ def run_ours(args):
                                       "peak_basis": f"dense TF32, {tsrc}",
                                       "note": "3 TF32 products per FP32 product; split passes included"}})
 
-    # end to end through the public call, host buffers, copies inside the timed region
+    # end to end through the public host-buffer call: sgemm_f32_host copies A and B
+    # from pinned host memory and C back, overlapped with the product over row
+    # panels; every copy is inside the timed region
     hA = torch.from_numpy(A).pin_memory()
     hB = torch.from_numpy(B).pin_memory()
     hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        step()
-        hC.copy_(dC, non_blocking=True)
+    panels = 8  # a hint: the library rounds panels up to whole waves of tiles
+    h_ws_bytes = sg.sgemm_f32_host_workspace_size(M, N, K, panels)
+    h_ws = torch.empty(max(h_ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    if args.path == "ffma":
+        def e2e_step():
+            sg.sgemm_f32_host(M, N, K, hA, K, hB, N, hC, N, panels, h_ws, h_ws_bytes, handle, s_in, s_out)
+    else:
+        def e2e_step():
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            step()
+            hC.copy_(dC, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -506,7 +516,9 @@ def run_ours(args):
     te_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e = {"value": job_tflops(flop, args.e2e_steps, world, te_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
-           "d2h_bytes_per_step": int(hC.numel() * 4), "steps": args.e2e_steps}
+           "d2h_bytes_per_step": int(hC.numel() * 4), "steps": args.e2e_steps,
+           "call": (f"sgemm_f32_host, {panels} row panels, copies overlapped with the product"
+                    if args.path == "ffma" else "host copies around the device call, serial")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -73,6 +73,11 @@ _SIGNATURES = {
                                   ctypes.c_void_p]),
     "sgemm_gemm_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_int, ctypes.c_int]),
+    "sgemm_f32_host": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "sgemm_f32_host_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     "sgemm_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
 }
@@ -245,6 +250,21 @@ def sgemm_gemm(algo: int, transa: int, transb: int, M: int, N: int, K: int, alph
 
 def sgemm_gemm_workspace_size(algo: int, transa: int, transb: int, M: int, N: int, K: int) -> int:
     return int(load().sgemm_gemm_workspace_size(int(algo), int(transa), int(transb), int(M), int(N), int(K)))
+
+
+def sgemm_f32_host(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int, panels: int, workspace,
+                   workspace_bytes: int, stream, h2d_stream, d2h_stream) -> None:
+    """C = A * B with host-memory A, B, C, copies overlapped with the product
+    (include/sgemm.h).  Pointers are ints or tensors (pinned CPU tensors for overlap)."""
+    lib = load()
+    st = lib.sgemm_f32_host(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
+                            int(panels), _ptr(workspace), int(workspace_bytes), _stream(stream), _stream(h2d_stream),
+                            _stream(d2h_stream))
+    _check(st, "sgemm_f32_host")
+
+
+def sgemm_f32_host_workspace_size(M: int, N: int, K: int, panels: int) -> int:
+    return int(load().sgemm_f32_host_workspace_size(int(M), int(N), int(K), int(panels)))
 
 
 def sgemm_device_status(stream=None) -> int:

@@ -552,6 +552,155 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
     return launch_product(p, 1, nullptr, 0, stream, info);
 }
 
+// ---------------------------------------------------------------- host buffers, pipelined
+
+namespace {
+
+struct HostPlan {
+    int rows;          // rows of C per panel (a multiple of the 128-row tile)
+    int panels;
+    int64_t lda_d;     // device row pitch of the A panels (floats)
+    int64_t ldn_d;     // device row pitch of B and of the C panels
+    size_t b_bytes, a_bytes, c_bytes, total;
+};
+
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// Panel height: about M / panels rows, rounded up to whole waves of output
+// tiles (the panels run one after another, so a panel that ends in a partly
+// filled wave leaves SMs idle at every panel boundary).
+HostPlan host_plan(int M, int N, int K, int panels, int sms) {
+    HostPlan h{};
+    if (panels < 1) panels = 1;
+    const int64_t tiles_n = (N + TmaTile::BN - 1) / TmaTile::BN;
+    const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * TmaTile::MIN_BLOCKS;
+    const int64_t wave_rows = (int64_t)TmaTile::BM * (slots / gcd64(slots, tiles_n > 0 ? tiles_n : 1));
+    int64_t rows = ((int64_t)M + panels - 1) / panels;
+    rows = (rows + wave_rows - 1) / wave_rows * wave_rows;
+    if (rows > M) rows = M;
+    if (rows < 1) rows = 1;
+    h.rows = (int)rows;
+    h.panels = (int)((M + rows - 1) / rows);
+    h.lda_d = ld4(K);
+    h.ldn_d = ld4(N);
+    h.b_bytes = (size_t)K * h.ldn_d * sizeof(float);
+    h.a_bytes = (size_t)rows * h.lda_d * sizeof(float);
+    h.c_bytes = (size_t)rows * h.ldn_d * sizeof(float);
+    // B once, two A panels and two C panels (double buffering), each 256-byte aligned
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    h.total = up(h.b_bytes) + 2 * up(h.a_bytes) + 2 * up(h.c_bytes);
+    return h;
+}
+
+}  // namespace
+
+size_t sgemm_f32_host_workspace_size(int M, int N, int K, int panels) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return 0;
+    return host_plan(M, N, K, panels, info.sms).total;
+}
+
+int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                   int panels, float *workspace, size_t workspace_bytes, cudaStream_t stream,
+                   cudaStream_t h2d_stream, cudaStream_t d2h_stream) {
+    if (M < 0 || N < 0 || K < 0 || panels < 1) return SGEMM_ERR_INVALID_ARG;
+    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1)) return SGEMM_ERR_INVALID_ARG;
+    if (((int64_t)M * K > 0 && !A) || ((int64_t)K * N > 0 && !B) || ((int64_t)M * N > 0 && !C))
+        return SGEMM_ERR_INVALID_ARG;
+    if ((int64_t)M * N == 0) return SGEMM_OK;
+    if (K == 0) {
+        // an empty sum: zero the host rows directly
+        for (int64_t i = 0; i < M; ++i)
+            for (int64_t j = 0; j < N; ++j) C[i * ldc + j] = 0.f;
+        return SGEMM_OK;
+    }
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    const HostPlan h = host_plan(M, N, K, panels, info.sms);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < h.total) return SGEMM_ERR_INVALID_ARG;
+
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    char *base = reinterpret_cast<char *>(workspace);
+    float *dB = reinterpret_cast<float *>(base);
+    float *dA[2] = {reinterpret_cast<float *>(base + up(h.b_bytes)),
+                    reinterpret_cast<float *>(base + up(h.b_bytes) + up(h.a_bytes))};
+    float *dC[2] = {reinterpret_cast<float *>(base + up(h.b_bytes) + 2 * up(h.a_bytes)),
+                    reinterpret_cast<float *>(base + up(h.b_bytes) + 2 * up(h.a_bytes) + up(h.c_bytes))};
+
+    // events: call start; B landed; A panel landed; A panel consumed; C panel
+    // ready; C panel copied out
+    cudaEvent_t ev_start, ev_b, ev_a[2], ev_a_free[2], ev_c[2], ev_c_free[2];
+    cudaEvent_t *all[] = {&ev_start, &ev_b, &ev_a[0], &ev_a[1], &ev_a_free[0], &ev_a_free[1],
+                          &ev_c[0], &ev_c[1], &ev_c_free[0], &ev_c_free[1]};
+    int made = 0;
+    int st = SGEMM_OK;
+    for (cudaEvent_t *e : all) {
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+            st = SGEMM_ERR_LAUNCH;
+            break;
+        }
+        ++made;
+    }
+    auto ok = [&](cudaError_t e) {
+        if (e != cudaSuccess && st == SGEMM_OK) st = SGEMM_ERR_LAUNCH;
+        return st == SGEMM_OK;
+    };
+    if (st == SGEMM_OK) {
+        // everything already queued on `stream` (an earlier call on the same
+        // workspace included) comes before this call's copies
+        ok(cudaEventRecord(ev_start, stream));
+        ok(cudaStreamWaitEvent(h2d_stream, ev_start, 0));
+        ok(cudaStreamWaitEvent(d2h_stream, ev_start, 0));
+        ok(cudaMemcpy2DAsync(dB, h.ldn_d * sizeof(float), B, (size_t)ldb * sizeof(float), (size_t)N * sizeof(float),
+                             K, cudaMemcpyHostToDevice, h2d_stream));
+        ok(cudaEventRecord(ev_b, h2d_stream));
+        ok(cudaStreamWaitEvent(stream, ev_b, 0));
+    }
+    for (int p = 0; p < h.panels && st == SGEMM_OK; ++p) {
+        const int b = p & 1;
+        const int r0 = p * h.rows;
+        const int rows = (M - r0) < h.rows ? (M - r0) : h.rows;
+        // copy A rows r0 .. r0 + rows - 1 once the product two panels back has read its buffer
+        if (p >= 2) ok(cudaStreamWaitEvent(h2d_stream, ev_a_free[b], 0));
+        ok(cudaMemcpy2DAsync(dA[b], h.lda_d * sizeof(float), A + (int64_t)r0 * lda, (size_t)lda * sizeof(float),
+                             (size_t)K * sizeof(float), rows, cudaMemcpyHostToDevice, h2d_stream));
+        ok(cudaEventRecord(ev_a[b], h2d_stream));
+        // the product, once its A panel has landed and its C buffer has been copied out
+        ok(cudaStreamWaitEvent(stream, ev_a[b], 0));
+        if (p >= 2) ok(cudaStreamWaitEvent(stream, ev_c_free[b], 0));
+        if (st != SGEMM_OK) break;
+        const Problem prob{rows, N, K, dA[b], (int)h.lda_d, dB, (int)h.ldn_d, dC[b], (int)h.ldn_d};
+        const int ls = launch_product(prob, 1, nullptr, 0, stream, info);
+        if (ls != SGEMM_OK) {
+            st = ls;
+            break;
+        }
+        ok(cudaEventRecord(ev_a_free[b], stream));
+        ok(cudaEventRecord(ev_c[b], stream));
+        // copy the C panel back to the host rows
+        ok(cudaStreamWaitEvent(d2h_stream, ev_c[b], 0));
+        ok(cudaMemcpy2DAsync(C + (int64_t)r0 * ldc, (size_t)ldc * sizeof(float), dC[b], h.ldn_d * sizeof(float),
+                             (size_t)N * sizeof(float), rows, cudaMemcpyDeviceToHost, d2h_stream));
+        ok(cudaEventRecord(ev_c_free[b], d2h_stream));
+    }
+    // `stream` completes only after the last copy out (and the copy streams' work)
+    if (st == SGEMM_OK) {
+        const int last = (h.panels - 1) & 1;
+        ok(cudaStreamWaitEvent(stream, ev_c_free[last], 0));
+        if (h.panels >= 2) ok(cudaStreamWaitEvent(stream, ev_c_free[last ^ 1], 0));
+    }
+    for (int i = 0; i < made; ++i) cudaEventDestroy(*all[i]);
+    return st;
+}
+
 int sgemm_device_status(cudaStream_t stream) {
     DeviceInfo info;
     if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;

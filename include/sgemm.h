@@ -215,6 +215,40 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K,
 size_t sgemm_gemm_workspace_size(int algo, int transa, int transb, int M, int N, int K);
 
 /*
+ * C = A * B with A, B and C in HOST memory: the end-to-end form of sgemm_f32.
+ * B is copied to the device once; then, panel by panel of at most `panels`
+ * row panels of C (each rounded up to whole waves of 128 x 128 output tiles
+ * on this device, so fewer panels may result), the rows of A are copied in
+ * on h2d_stream, the product runs on `stream` with the kernels of sgemm_f32,
+ * and the rows of C are copied back on d2h_stream, so that copies of one panel
+ * overlap the product of another.  Every element of C is computed exactly as
+ * sgemm_f32 computes it.
+ *   workspace: caller-owned device memory of at least
+ *     sgemm_f32_host_workspace_size(M, N, K, panels) bytes (B, two A panels
+ *     and two C panels), 16-byte aligned; the library allocates nothing.
+ *   streams: three caller-owned streams (distinct for overlap); the copies
+ *     start only after the work already queued on `stream` (so back-to-back
+ *     calls may share one workspace); the call is asynchronous and its work
+ *     is complete when `stream` reaches the point after the call (synchronise
+ *     `stream`, not the copy streams).  A, B and
+ *     C must stay valid until then; pinned (page-locked) host memory is needed
+ *     for the copies to overlap.  It creates and releases a few CUDA events.
+ *   K == 0: C's rows are zeroed on the host before returning.
+ * Errors: SGEMM_ERR_INVALID_ARG (sizes, strides, NULL, panels < 1, short or
+ * misaligned workspace), SGEMM_ERR_LAUNCH (a copy, event or launch failed).
+ */
+int sgemm_f32_host(int M, int N, int K,
+                   const float *A, int lda,
+                   const float *B, int ldb,
+                   float *C, int ldc,
+                   int panels, float *workspace, size_t workspace_bytes,
+                   cudaStream_t stream, cudaStream_t h2d_stream, cudaStream_t d2h_stream);
+
+/* Device workspace bytes sgemm_f32_host needs for this shape and panel count
+ * on the current device (it queries the SM count; 0 if that fails). */
+size_t sgemm_f32_host_workspace_size(int M, int N, int K, int panels);
+
+/*
  * The pages' kernel ladder, as GPU kernels: the reference points the tuned
  * kernels are measured against, and the kernels whose executed global loads
  * the pages count.  Every level computes C = A * B with the same contract,
