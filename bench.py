@@ -70,7 +70,7 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
-    p.add_argument("--path", choices=["ffma", "splitk", "3xtf32"] + sorted(LADDER), default="ffma",
+    p.add_argument("--path", choices=["ffma", "splitk", "3xtf32", "gemm"] + sorted(LADDER), default="ffma",
                    help="ffma: sgemm_f32 (the headline); splitk: sgemm_f32_splitk with the suggested split "
                         "count; 3xtf32: sgemm_f32_3xtf32 (tensor cores). Workspaces are allocated untimed.")
     p.add_argument("--no-variants", action="store_true",
@@ -241,6 +241,15 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
         def step():
             sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
         return step, (2 if splits > 1 else 1)
+    if path == "gemm":
+        # sgemm_gemm, FFMA form: unaligned operands are repacked into the workspace
+        ws_bytes = sg.sgemm_gemm_workspace_size(0, 0, 0, M, N, K)
+        ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+        cfg["path"] = "sgemm_gemm (FFMA; operands repacked when unaligned)"
+
+        def step():
+            sg.sgemm_gemm(0, 0, 0, M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, ws, ws_bytes, handle)
+        return step, 1
     if path in LADDER:
         cfg["path"] = path
 

@@ -32,6 +32,7 @@ namespace {
 // 128 x 128 CTA tile, 16-deep k-steps, 4 cp.async stages, 2 CTAs per SM.
 using CpTile = sgemm::FfmaTile<128, 128, 16, 4, 2>;
 using TmaTile = sgemm::TmaMainTile;
+using TmaSmallK = sgemm::TmaSmallKTile;
 using X3Tile = sgemm::Tf32x3MainTile;
 
 constexpr int kMaxDevices = 64;
@@ -148,6 +149,21 @@ bool cp_attr(int dev) {
     return smem_attr_once(done[dev], sgemm::sgemm_ffma_kernel<T, VB, VC>, T::SMEM_BYTES);
 }
 
+template <class T>
+int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
+               cudaStream_t stream, const DeviceInfo &info) {
+    alignas(64) CUtensorMap ta, tb;
+    if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return SGEMM_ERR_LAUNCH;
+    if (!(vc ? tma_attr<T, true>(info.dev) : tma_attr<T, false>(info.dev))) return SGEMM_ERR_LAUNCH;
+    auto kernel = vc ? sgemm::sgemm_ffma_tma_kernel<T, true> : sgemm::sgemm_ffma_tma_kernel<T, false>;
+    const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
+    kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc, partials, ldp,
+                                                        info.err_word, g_wait_limit_ns.load(), g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Launch the product kernel over a (tiles x splits) grid.  splits > 1 writes
 // partial sums to `partials` (splits slabs of M x ldp) instead of C.
 int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
@@ -156,17 +172,9 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     // partial slabs hold the raw products; alpha and beta act in the reduction
     const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
     if (use_tma(p)) {
-        using T = TmaTile;
-        alignas(64) CUtensorMap ta, tb;
-        if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return SGEMM_ERR_LAUNCH;
-        if (!(vc ? tma_attr<T, true>(info.dev) : tma_attr<T, false>(info.dev))) return SGEMM_ERR_LAUNCH;
-        auto kernel = vc ? sgemm::sgemm_ffma_tma_kernel<T, true> : sgemm::sgemm_ffma_tma_kernel<T, false>;
-        const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
-        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc, partials, ldp,
-                                                            info.err_word, g_wait_limit_ns.load(),
-                                                            g_debug_flags.load());
+        if (splits == 1 && p.K <= 2 * TmaSmallK::BK)
+            return launch_tma<TmaSmallK>(p, alpha, beta, vc, splits, partials, ldp, stream, info);
+        return launch_tma<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, stream, info);
     } else {
         using T = CpTile;
         const bool vb = aligned16(p.B) && p.ldb % 4 == 0;
@@ -230,14 +238,12 @@ int ld_partials(int N) { return ((N + 3) / 4) * 4; }
 
 int64_t ld4(int n) { return ((int64_t)n + 3) / 4 * 4; }
 
-// Workspace of the FFMA form of sgemm_gemm: row-major copies of the operands
-// given transposed (A^T -> M x K, B^T -> K x N, rows padded to 4 floats).
-size_t gemm_ffma_workspace(int transa, int transb, int M, int N, int K) {
+// Workspace of the FFMA form of sgemm_gemm: room for row-major copies of both
+// operands (A -> M x K, B -> K x N, rows padded to 4 floats), used for an
+// operand given transposed or not 16-byte aligned (base or leading dimension).
+size_t gemm_ffma_workspace(int, int, int M, int N, int K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    size_t b = 0;
-    if (transa) b += (size_t)M * (size_t)ld4(K) * sizeof(float);
-    if (transb) b += (size_t)K * (size_t)ld4(N) * sizeof(float);
-    return b;
+    return ((size_t)M * (size_t)ld4(K) + (size_t)K * (size_t)ld4(N)) * sizeof(float);
 }
 
 size_t partials_bytes(int M, int N, int splits) {
@@ -515,7 +521,12 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
         sgemm::scale_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
         return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
     }
-    const size_t need = sgemm_gemm_workspace_size(algo, transa, transb, M, N, K);
+    // the FFMA form needs its workspace only for transposed or unaligned operands
+    const bool a_copy = transa || !aligned16(A) || lda % 4 != 0;
+    const bool b_copy = transb || !aligned16(B) || ldb % 4 != 0;
+    const size_t need = algo == SGEMM_ALGO_3XTF32 || a_copy || b_copy
+                            ? sgemm_gemm_workspace_size(algo, transa, transb, M, N, K)
+                            : 0;
     if (need > 0) {
         if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
         const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + need;
@@ -533,18 +544,28 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
         p.transb = transb == SGEMM_OP_T;
         return launch_3xtf32(p, workspace, stream, info);
     }
-    // FFMA: transposed operands are first copied row-major into the workspace
+    // FFMA: transposed operands are first copied row-major into the workspace,
+    // and operands whose base or rows are not 16-byte aligned are copied there
+    // with padded rows, so that the product runs on the TMA-fed kernel
     float *w = workspace;
-    if (transa) {
+    if (a_copy) {
         const int ld = (int)ld4(K);
-        sgemm::transpose_kernel<<<dim3((M + 31) / 32, (K + 31) / 32), 256, 0, stream>>>(K, M, A, lda, w, ld);
+        if (transa)
+            sgemm::transpose_kernel<<<dim3((M + 31) / 32, (K + 31) / 32), 256, 0, stream>>>(K, M, A, lda, w, ld);
+        else if (cudaMemcpy2DAsync(w, (size_t)ld * sizeof(float), A, (size_t)lda * sizeof(float),
+                                   (size_t)K * sizeof(float), M, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
         p.A = w;
         p.lda = ld;
-        w += (int64_t)M * ld;
     }
-    if (transb) {
+    w = workspace + (int64_t)M * ld4(K);
+    if (b_copy) {
         const int ld = (int)ld4(N);
-        sgemm::transpose_kernel<<<dim3((K + 31) / 32, (N + 31) / 32), 256, 0, stream>>>(N, K, B, ldb, w, ld);
+        if (transb)
+            sgemm::transpose_kernel<<<dim3((K + 31) / 32, (N + 31) / 32), 256, 0, stream>>>(N, K, B, ldb, w, ld);
+        else if (cudaMemcpy2DAsync(w, (size_t)ld * sizeof(float), B, (size_t)ldb * sizeof(float),
+                                   (size_t)N * sizeof(float), K, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return SGEMM_ERR_LAUNCH;
         p.B = w;
         p.ldb = ld;
     }

@@ -161,3 +161,27 @@ def test_bad_arguments(sg):
         sg.sgemm_gemm(0, 1, 0, 16, 8, 8, 1.0, x, 8, y, 8, 0.0, z, 8)
     with pytest.raises(sg.SgemmError):          # transposes on FFMA need a workspace
         sg.sgemm_gemm(0, 1, 0, 8, 8, 8, 1.0, x, 8, y, 8, 0.0, z, 8)
+
+
+@pytest.mark.parametrize("a_off,lda_pad,ldb_pad", [(1, 0, 0), (0, 1, 0), (0, 0, 3), (2, 5, 1)])
+def test_unaligned_operands_are_repacked(sg, a_off, lda_pad, ldb_pad):
+    # FFMA form with unaligned A or B: the product must not change, only its kernel
+    M, N, K = 190, 170, 150
+    A, B, C0 = stored(M, N, K, 0, 0, seed=117)
+    C = run_gemm(sg, 0, 0, 0, 1.0, A, B, 0.0, C0, lda=K + lda_pad, ldb=N + ldb_pad, a_off=a_off)
+    check_general(C, 0, 0, 1.0, A, B, 0.0, C0)
+
+
+def test_ragged_workload_through_sgemm_gemm(sg):
+    import torch
+    M, N, K, dist, seed = gen.WORKLOADS["ragged_3001x4999x2047"]
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.full((M, N), float("nan"), device="cuda")
+    need = sg.sgemm_gemm_workspace_size(0, 0, 0, M, N, K)
+    ws = torch.empty(need // 4, device="cuda")
+    sg.sgemm_gemm(0, 0, 0, M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, ws, need)
+    torch.cuda.synchronize()
+    C = dC.cpu().numpy()
+    from helpers import check_rows
+    check_rows(C, A, B, [0, 1, 127, 128, 2999, 3000] + list(np.random.default_rng(8).integers(0, M, 20)))
