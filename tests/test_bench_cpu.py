@@ -1,0 +1,56 @@
+"""The benchmark's CPU-side pieces: the reference arm (the CPU oracle) prints
+one JSON line with the contract's keys; the workload and roofline helpers."""
+
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_6x6x9",
+                          "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"].startswith("tiny_6x6x9")
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_6x6x9",
+                          "--steps", "3", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                         env=env)
+    assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_workload_config_and_metric_names():
+    M, N, K, dist, seed, cfg = bench.workload_config("square_8192")
+    assert (M, N, K, dist, seed) == (8192, 8192, 8192, "normal", 2)
+    assert "no flush" in cfg["l2"]
+    assert bench.metric_name("square_8192") == bench.METRIC
+    assert "M=1024" in bench.metric_name("square_1024")
+    assert "512 MB buffer is written between timed steps" in bench.workload_config("square_1024")[5]["l2"]
+
+
+def test_recorded_traffic_follows_the_kernel_sources():
+    # the committed ncu summary carries the digest of the kernel headers it was taken on
+    t = bench.recorded_traffic()
+    assert t is None or t > 805_306_368       # at least the algorithmic bytes when present
+    assert len(bench.kernel_source_digest()) == 16
+
+
+def test_tf32_peak_derivation():
+    peak, basis = bench.tf32_peak_tflops()
+    assert 400 < peak < 1200 and "1.1/2.25" in basis
