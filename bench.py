@@ -73,6 +73,8 @@ def parse_args():
     p.add_argument("--path", choices=["ffma", "splitk", "3xtf32", "gemm"] + sorted(LADDER), default="ffma",
                    help="ffma: sgemm_f32 (the headline); splitk: sgemm_f32_splitk with the suggested split "
                         "count; 3xtf32: sgemm_f32_3xtf32 (tensor cores). Workspaces are allocated untimed.")
+    p.add_argument("--no-context", action="store_true",
+                   help="skip the torch.matmul (cuBLAS SGEMM) context timing")
     p.add_argument("--no-variants", action="store_true",
                    help="skip the extra 3xTF32 measurement reported beside the headline")
     return p.parse_args()
@@ -240,7 +242,7 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
 
         def step():
             sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
-        return step, (2 if splits > 1 else 1)
+        return step, (2 if splits > 1 else f32_launches(sg, M, N, K))
     if path == "gemm":
         # sgemm_gemm, FFMA form: unaligned operands are repacked into the workspace
         ws_bytes = sg.sgemm_gemm_workspace_size(0, 0, 0, M, N, K)
@@ -249,7 +251,9 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
 
         def step():
             sg.sgemm_gemm(0, 0, 0, M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, ws, ws_bytes, handle)
-        return step, 1
+        # the product runs on 16-byte aligned (repacked if need be) operands: the
+        # TMA path's one or two launches; the repacking copies are not kernels of ours
+        return step, f32_launches(sg, M, N, K, aligned=True)
     if path in LADDER:
         cfg["path"] = path
 
@@ -267,7 +271,16 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
 
     def step():
         sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
-    return step, 1
+    return step, f32_launches(sg, M, N, K)
+
+
+def f32_launches(sg, M, N, K, aligned=False):
+    """Kernels one sgemm_f32 call launches for contiguous operands: one, or two
+    when a cluster-split grid follows whole rounds of plain tiles."""
+    if K > 64 and (aligned or (K % 4 == 0 and N % 4 == 0)):
+        tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
+        return 2 if cs > 1 and 0 < full < tiles else 1
+    return 1
 
 
 def tf32_peak_tflops():
@@ -292,11 +305,19 @@ def time_steps(step, steps, stream, dev):
     return e0.elapsed_time(e1)
 
 
-def kernel_name(M, N, K):
+def kernel_name(sg, M, N, K):
     """The kernel sgemm_f32 launches for a contiguous M x K by K x N product."""
     if K > 0 and K % 4 == 0 and N % 4 == 0:
-        return ("sgemm_ffma_tma_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as fma.rn.f32x2 "
+        if K <= 64:
+            return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed small-K tile, 1 stage, 8x8 per thread as "
+                    "fma.rn.f32x2 column pairs, 3 CTAs/SM)")
+        name = ("sgemm_ffma_tma_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as fma.rn.f32x2 "
                 "column pairs, 2 CTAs/SM)")
+        tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
+        if cs > 1:
+            name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
+                     "added through distributed shared memory)")
+        return name
     return "sgemm_ffma_kernel (128x128x16 cp.async tile, 4 stages, 8x8 per thread)"
 
 
@@ -446,7 +467,7 @@ def run_ours(args):
     roofline["algorithmic_bytes"] = alg_bytes
     roofline["alu_floor_ms"] = t_alu * 1e3
     roofline["hbm_floor_ms"] = t_hbm * 1e3
-    roofline["kernel"] = kernel_name(M, N, K) + (f" + split-K x{cfg['splitk']} with reduction"
+    roofline["kernel"] = kernel_name(sg, M, N, K) + (f" + split-K x{cfg['splitk']} with reduction"
                                                  if cfg.get("splitk", 1) > 1 else "")
     if args.path in LADDER:
         roofline["kernel"] = f"{args.path} (the pages' kernel ladder)"
@@ -488,6 +509,26 @@ def run_ours(args):
                                       "unit": "TFLOP/s", "frac": 3 * vval / world / tpk,
                                       "peak_basis": f"dense TF32, {tsrc}",
                                       "note": "3 TF32 products per FP32 product; split passes included"}})
+
+    # context, not this library: cuBLAS SGEMM through torch.matmul with TF32 off,
+    # on the same inputs, timed the same way (outside the timed region)
+    context = None
+    if args.path == "ffma" and not args.no_context and K > 0:
+        prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        dC2 = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+        def cublas_step():
+            torch.matmul(dA, dB, out=dC2)
+        for _ in range(3):
+            cublas_step()
+        csteps = max(5, args.steps // 2)
+        ct = max_over_ranks(time_steps(cublas_step, csteps, stream, dev), world, dev)
+        torch.backends.cuda.matmul.allow_tf32 = prev
+        context = {"what": "torch.matmul with TF32 off (cuBLAS SGEMM); context only, not this library",
+                   "value": job_tflops(flop, csteps, world, ct), "unit": "TFLOP/s", "ms_per_step": ct / csteps,
+                   "steps": csteps, "l2_flushed_between_steps": False}
+        del dC2
 
     # end to end through the public host-buffer call: sgemm_f32_host copies A and B
     # from pinned host memory and C back, overlapped with the product over row
@@ -541,7 +582,7 @@ def run_ours(args):
             "config": cfg, "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples",
                                                                 "power_w_max")},
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * launches_per_step, "cpu_baseline": cpu,
-            "check": check, "device": props.name, "sms": sms, "variants": variants,
+            "check": check, "device": props.name, "sms": sms, "variants": variants, "context": context,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

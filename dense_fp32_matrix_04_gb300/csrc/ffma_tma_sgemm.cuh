@@ -31,6 +31,18 @@
 //    16-byte chunks of B (broadcast) and at most four of A.
 //  * Every wait on an mbarrier is bounded; on a timeout the CTA leaves the loop
 //    together, records an error code in device memory and writes nothing.
+//  * Cluster split: for grids that leave SMs idle -- few tiles, or a last
+//    partial wave -- the CTAs of a thread-block cluster of 2 to 8 share one
+//    tile, each taking an equal run of k-steps.  Every CTA
+//    parks its partial sums in its own (now idle) stage buffers; after a
+//    cluster barrier, rank r reads its share of the tile's rows from every
+//    rank's shared memory in rank order (distributed shared memory), adds them
+//    in that fixed order and stores those rows.  No workspace, no atomics, and
+//    the same bits on every run.  When full waves of plain tiles come first,
+//    the cluster-split grid is launched as a programmatic dependent of theirs:
+//    its CTAs take SMs as the last plain CTAs drain instead of after all of
+//    them, and each waits for the plain grid to complete before it exits, so
+//    the pair completes as one product.
 #pragma once
 
 #include <cuda.h>
@@ -68,6 +80,8 @@ struct TmaTile {
     static constexpr int B_STAGE = BK * BN * 4;  // BK dense rows of BN floats
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 /* alignment slack */ + 8 * STAGES /* barriers */;
+    // the cluster split parks a CTA's packed partial sums (and a flag word) in its stage buffers
+    static constexpr bool CSPLIT_OK = PACKED && TM * TN * THREADS * 4 + 16 <= STAGES * STAGE;
     static_assert(TN % 4 == 0, "columns come in 4-wide quads");
     static_assert(BM <= 256 && BN <= 256, "a TMA box spans at most 256 elements per dimension");
     static_assert(BK * 4 == 128, "A rows must be exactly one 128-byte swizzle span");
@@ -99,12 +113,24 @@ enum : int { kDeviceErrNone = 0, kDeviceErrTimeout = 1 };
 // bounded waits run out.
 enum : int { kDebugSkipCopies = 1 };
 
-template <class T, bool VEC_C>
+// What a launch of the kernel does: a plain grid of tiles; the same, as the
+// first of a plain + cluster-split pair (it lets the second grid start early);
+// or the cluster-split grid.
+enum : int { kRolePlain = 0, kRolePrimary = 1, kRoleSplit = 2 };
+
+// Tile t of the launch is grouped tile tile_base + blockIdx.x (tile_base +
+// cluster index for the split role), so one product can be covered by a plain
+// launch over tiles [0, full) and a cluster-split launch over [full, tiles).
+template <class T, bool VEC_C, int ROLE = kRolePlain>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M,
                           int N, int K, float alpha, float beta, float *__restrict__ C, int ldc,
-                          float *__restrict__ partials, int ldp, int *__restrict__ err_word,
+                          float *__restrict__ partials, int ldp, int tile_base, int *__restrict__ err_word,
                           unsigned long long wait_limit_ns, int debug) {
+    constexpr bool CSPLIT = ROLE == kRoleSplit;
+    static_assert(!CSPLIT || T::CSPLIT_OK, "the cluster split exchanges packed accumulators through the stage buffers");
+    // the cluster-split grid queued behind this one may start as soon as all of its CTAs run
+    if constexpr (ROLE == kRolePrimary) griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern
     const uint32_t raw = smem_addr(smem_raw);
@@ -118,18 +144,23 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
 
     const int tiles_m = (M + T::BM - 1) / T::BM;
     const int tiles_n = (N + T::BN - 1) / T::BN;
+    // cluster split: `cs` CTAs share a tile; this one is rank `rank`
+    const int cs = CSPLIT ? (int)cluster_nctarank() : 1;
+    const int rank = CSPLIT ? (int)cluster_ctarank() : 0;
     int tile_m, tile_n;
-    grouped_tile<8>(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
+    grouped_tile<8>(tile_base + (CSPLIT ? (int)cluster_id_x() : (int)blockIdx.x), tiles_m, tiles_n, tile_m, tile_n);
     const int m0 = tile_m * T::BM;
     const int n0 = tile_n * T::BN;
-    // split-K: CTA row blockIdx.y owns k-steps [kt_begin, kt_begin + KT) and, when
-    // the grid has more than one row, writes its partial sums to its own M x N
-    // slab of `partials` (leading dimension ldp) instead of C
+    // split-K: CTA row blockIdx.y (or cluster rank) owns k-steps [kt_begin,
+    // kt_begin + KT).  A grid with more than one row writes its partial sums to
+    // its own M x N slab of `partials` (leading dimension ldp) instead of C.
     const int KT_all = (K + T::BK - 1) / T::BK;
-    const int per_split = (KT_all + gridDim.y - 1) / gridDim.y;
-    const int kt_begin = blockIdx.y * per_split;
+    const int parts = CSPLIT ? cs : (int)gridDim.y;
+    const int part = CSPLIT ? rank : (int)blockIdx.y;
+    const int per_split = (KT_all + parts - 1) / parts;
+    const int kt_begin = part * per_split;
     const int KT = max(0, min(KT_all, kt_begin + per_split) - kt_begin);
-    if (gridDim.y > 1) {
+    if (!CSPLIT && gridDim.y > 1) {
         C = partials + (int64_t)blockIdx.y * M * ldp;
         ldc = ldp;
     }
@@ -279,7 +310,66 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                     (void)mbar_wait_bounded(bars + 8 * (t % T::STAGES), (t / T::STAGES) & 1, wait_limit_ns);
         }
         __syncthreads();
-        return;
+        // a cluster-split CTA still takes part in both cluster barriers below
+        if constexpr (!CSPLIT) return;
+    }
+
+    if constexpr (CSPLIT) {
+        // 16-byte chunk c = i * TN/4 + q (accumulator pairs 2q, 2q + 1 of row i) of
+        // thread tid sits at (c * THREADS + tid) * 16 in the stage buffers, which
+        // every warp has finished reading (the loop's last barrier); a word after
+        // the chunks says whether this CTA gave up on a wait
+        constexpr int CHUNKS = T::TM * T::TN / 4;
+        const uint32_t flag = base + CHUNKS * T::THREADS * 16;
+        if (failed_kt < 0) {
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+                for (int q = 0; q < T::TN / 4; ++q)
+                    *reinterpret_cast<ulonglong2 *>(smem + ((i * (T::TN / 4) + q) * T::THREADS + tid) * 16) =
+                        make_ulonglong2(acc2[i][2 * q], acc2[i][2 * q + 1]);
+        }
+        if (tid == 0) *reinterpret_cast<volatile uint32_t *>(smem + CHUNKS * T::THREADS * 16) = failed_kt >= 0;
+        cluster_sync();
+        uint32_t bad = 0;
+        for (int r = 0; r < cs; ++r) bad |= dsmem_ld_u32(dsmem_map(flag, (uint32_t)r));
+        if (!bad) {
+            const uint64_t one2 = f32x2_dup(1.f);
+            // rows i with i * cs / TM == rank are this CTA's share (cs <= TM): the sum over
+            // ranks 0, 1, ..., cs - 1 in that order, whichever CTA computes it
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i) {
+                if ((i * cs) / T::TM != rank) continue;
+#pragma unroll
+                for (int q = 0; q < T::TN / 4; ++q) {
+                    const uint32_t off = base + ((i * (T::TN / 4) + q) * T::THREADS + tid) * 16;
+                    uint64_t s0 = acc2[i][2 * q], s1 = acc2[i][2 * q + 1];
+                    if (rank != 0) {
+                        const ulonglong2 v = dsmem_ld_v2u64(dsmem_map(off, 0));
+                        s0 = v.x;
+                        s1 = v.y;
+                    }
+                    for (int r = 1; r < cs; ++r) {
+                        uint64_t v0 = acc2[i][2 * q], v1 = acc2[i][2 * q + 1];
+                        if (r != rank) {
+                            const ulonglong2 v = dsmem_ld_v2u64(dsmem_map(off, (uint32_t)r));
+                            v0 = v.x;
+                            v1 = v.y;
+                        }
+                        f32x2_fma(s0, v0, one2);  // s + v, rounded once (v * 1 is exact)
+                        f32x2_fma(s1, v1, one2);
+                    }
+                    acc2[i][2 * q] = s0;
+                    acc2[i][2 * q + 1] = s1;
+                }
+            }
+        }
+        // the other CTAs' shared memory must stay in place until every rank has read it
+        cluster_sync();
+        if (bad) {
+            griddep_wait();
+            return;
+        }
     }
 
     // epilogue: rows row0 + 8 i, 16-byte column quads at col0 + 16 q;
@@ -288,6 +378,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     for (int i = 0; i < T::TM; ++i) {
         const int row = m0 + row0 + 8 * i;
         if (row >= M) continue;
+        if (CSPLIT && (i * cs) / T::TM != rank) continue;
         float *crow = C + (int64_t)row * ldc;
 #pragma unroll
         for (int q = 0; q < T::TN / 4; ++q) {
@@ -303,6 +394,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
             store_quad<VEC_C>(crow, col, N, vp, alpha, beta);
         }
     }
+    // a cluster-split grid overlapping a plain one completes after it
+    if constexpr (CSPLIT) griddep_wait();
 }
 
 }  // namespace sgemm

@@ -53,6 +53,64 @@ __device__ __forceinline__ void f32x2_fma(uint64_t &d, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;\n" : "+l"(d) : "l"(a), "l"(b));
 }
 
+// ---------------------------------------------------------------- thread-block clusters (sm_90+)
+
+// Rank of this CTA in its cluster, and the cluster's CTA count (1 and 0 when
+// the launch has no cluster dimension).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+    return r;
+}
+// Index of this CTA's cluster along x in the grid.
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;\n" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives (release) and waits
+// (acquire): shared-memory writes made before it are visible to the other
+// CTAs' distributed shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Address, in the cluster's shared window, of the word at CTA-local shared
+// address `addr` in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ ulonglong2 dsmem_ld_v2u64(uint32_t cluster_addr) {
+    ulonglong2 v;
+    asm volatile("ld.shared::cluster.v2.u64 {%0, %1}, [%2];\n" : "=l"(v.x), "=l"(v.y) : "r"(cluster_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch (sm_90+)
+
+// Let the next grid in the stream, if it was launched with programmatic stream
+// serialization, start once every CTA of this grid has passed this point.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n");
+}
+// Wait until the grids this one may overlap have completed and their memory
+// operations are visible (returns at once when there are none).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier / TMA (sm_90+)
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

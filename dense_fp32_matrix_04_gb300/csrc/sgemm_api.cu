@@ -38,8 +38,15 @@ using X3Tile = sgemm::Tf32x3MainTile;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 64;
 
-// test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernel
+// test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernel.
+// Bits 4..7: cluster size forced on the TMA path's cluster split (0 = the
+// automatic plan, 1 = never split, 2 .. 8 = split the tiles beyond whole
+// multiples of the SM count with that cluster size); bit 8: put every tile in
+// the cluster-split launch; bit 9 below.
 constexpr int kDebugForceCpAsync = 2;
+constexpr int kDebugClusterShift = 4;
+constexpr int kDebugClusterAll = 256;
+constexpr int kDebugNoOverlap = 512;  // launch the cluster-split grid without programmatic overlap
 std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
@@ -137,10 +144,10 @@ int k_tiles(const Problem &p) {
     return (p.K + bk - 1) / bk;
 }
 
-template <class T, bool VC>
+template <class T, bool VC, int ROLE>
 bool tma_attr(int dev) {
     static std::atomic<int> done[kMaxDevices];
-    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC>, T::SMEM_BYTES);
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC, ROLE>, T::SMEM_BYTES);
 }
 
 template <class T, bool VB, bool VC>
@@ -149,19 +156,164 @@ bool cp_attr(int dev) {
     return smem_attr_once(done[dev], sgemm::sgemm_ffma_kernel<T, VB, VC>, T::SMEM_BYTES);
 }
 
+// The cluster-split launch configuration: `clusters` clusters of cs CTAs and,
+// after a plain grid of the same product, programmatic overlap with that grid.
+template <class T>
+cudaLaunchConfig_t split_config(int64_t clusters, int cs, bool overlap, cudaStream_t stream,
+                                cudaLaunchAttribute (&attr)[2]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(clusters * cs));
+    cfg.blockDim = dim3(T::THREADS);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 2 : 1;
+    return cfg;
+}
+
+// Whether clusters of `cs` CTAs of the cluster-split kernel can be resident on
+// this device at all; queried once per device and size.
+template <class T>
+bool cluster_fits(int dev, int cs) {
+    static std::atomic<int> known[kMaxDevices][9];  // 0 unknown, 1 yes, 2 no
+    if (cs < 2 || cs > 8) return false;
+    std::atomic<int> &slot = known[dev][cs];
+    int k = slot.load(std::memory_order_acquire);
+    if (k == 0) {
+        if (!tma_attr<T, true, sgemm::kRoleSplit>(dev)) return false;
+        cudaLaunchAttribute attr[2];
+        const cudaLaunchConfig_t cfg = split_config<T>(1, cs, false, 0, attr);
+        int n = 0;
+        const bool ok =
+            cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit>, &cfg) ==
+                cudaSuccess &&
+            n > 0;
+        if (!ok) (void)cudaGetLastError();
+        k = ok ? 1 : 2;
+        slot.store(k, std::memory_order_release);
+    }
+    return k == 1;
+}
+
+// How a product on the TMA main tile is launched: tiles [0, full) as a plain
+// grid, tiles [full, tiles) as clusters of `cs` CTAs that split each tile's
+// k-steps (cs == 1: no cluster split).
+struct SplitPlan {
+    int64_t tiles = 0;
+    int64_t full = 0;
+    int cs = 1;
+};
+
+// Cost model of the main tile, fitted to measurements on GB300 of products from
+// 512 x 512 x 8192 to 8192^3: two CTAs on an SM each advance one k-step per
+// unit of time; one CTA alone on an SM advances two (the SM's throughput is
+// the same); and each CTA spends kCtaOverheadSteps units outside its k-loop
+// (pipeline fill, epilogue, partial-sum exchange), hidden behind the other
+// CTA's work when two share the SM.
+constexpr double kCtaOverheadSteps = 2.0;
+
+// Time for an SM to run L CTAs of w k-steps each, two at a time and the last
+// one alone when L is odd.
+double sm_time(int64_t L, double w) {
+    return (double)(L / 2) * (w + kCtaOverheadSteps) + (double)(L % 2) * (0.5 * w + kCtaOverheadSteps);
+}
+
+// The cluster split fills SMs that a grid would leave idle.  With P SMs, the
+// `rem` tiles beyond whole multiples of P (all of them when there are fewer
+// than P) are shared by clusters of c = 2, 4 or 8 CTAs -- c chosen by the cost
+// model among those leaving at least four 32-deep k-steps per CTA, ties to the
+// larger c -- when the estimate beats the plain grid by 4 % or more.
+SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info) {
+    using T = TmaTile;
+    SplitPlan plan;
+    plan.tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
+    plan.full = plan.tiles;
+    const int64_t P = info.sms;
+    const int64_t kt = (K + T::BK - 1) / T::BK;
+    if (P <= 0 || plan.tiles == 0) return plan;
+    const int dbg = g_debug_flags.load();
+    const int forced = (dbg >> kDebugClusterShift) & 15;
+    const int64_t rem = plan.tiles % P;
+    int64_t full = plan.tiles - rem;
+    int cs = 1;
+    if (forced) {
+        cs = forced;
+        if (dbg & kDebugClusterAll) full = 0;
+    } else if (rem > 0) {
+        const double plain = sm_time((plan.tiles + P - 1) / P, (double)kt);
+        double best = plain;
+        for (int c = 2; c <= 8 && kt >= 4 * c; c *= 2) {
+            const double t = sm_time(full / P, (double)kt) + sm_time((rem * c + P - 1) / P, (double)((kt + c - 1) / c));
+            if (t <= best) best = t, cs = c;
+        }
+        if (cs > 1 && best > 0.96 * plain) cs = 1;
+    }
+    if (cs < 2 || cs > 8 || full == plan.tiles) return plan;
+    if (!cluster_fits<T>(info.dev, cs)) return plan;
+    plan.full = full;
+    plan.cs = cs;
+    return plan;
+}
+
+// Launch the TMA kernel over grouped tiles [tile_base, tile_base + tiles): a
+// plain (tiles x splits) grid, the same as the first of a plain + split pair
+// (primary), or tiles clusters of cs CTAs (cs > 1).
 template <class T>
 int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
-               cudaStream_t stream, const DeviceInfo &info) {
+               int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
     alignas(64) CUtensorMap ta, tb;
     if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
         return SGEMM_ERR_LAUNCH;
-    if (!(vc ? tma_attr<T, true>(info.dev) : tma_attr<T, false>(info.dev))) return SGEMM_ERR_LAUNCH;
-    auto kernel = vc ? sgemm::sgemm_ffma_tma_kernel<T, true> : sgemm::sgemm_ffma_tma_kernel<T, false>;
-    const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
-    kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc, partials, ldp,
-                                                        info.err_word, g_wait_limit_ns.load(), g_debug_flags.load());
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    const unsigned long long wait = g_wait_limit_ns.load();
+    const int dbg = g_debug_flags.load();
+    using sgemm::sgemm_ffma_tma_kernel;
+    if (cs <= 1) {
+        const dim3 grid((unsigned)tiles, (unsigned)splits);
+        if (primary) {
+            if constexpr (!T::CSPLIT_OK) {
+                return SGEMM_ERR_LAUNCH;  // only a tile that supports the cluster split has a split to precede
+            } else {
+                if (!(vc ? tma_attr<T, true, sgemm::kRolePrimary>(info.dev)
+                         : tma_attr<T, false, sgemm::kRolePrimary>(info.dev)))
+                    return SGEMM_ERR_LAUNCH;
+                auto kernel = vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRolePrimary>
+                                 : sgemm_ffma_tma_kernel<T, false, sgemm::kRolePrimary>;
+                kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc,
+                                                                    partials, ldp, (int)tile_base, info.err_word, wait,
+                                                                    dbg);
+            }
+        } else {
+            if (!(vc ? tma_attr<T, true, sgemm::kRolePlain>(info.dev) : tma_attr<T, false, sgemm::kRolePlain>(info.dev)))
+                return SGEMM_ERR_LAUNCH;
+            auto kernel = vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRolePlain>
+                             : sgemm_ffma_tma_kernel<T, false, sgemm::kRolePlain>;
+            kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc,
+                                                                partials, ldp, (int)tile_base, info.err_word, wait, dbg);
+        }
+        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
+    if constexpr (!T::CSPLIT_OK) {
+        return SGEMM_ERR_LAUNCH;
+    } else {
+        if (!(vc ? tma_attr<T, true, sgemm::kRoleSplit>(info.dev) : tma_attr<T, false, sgemm::kRoleSplit>(info.dev)))
+            return SGEMM_ERR_LAUNCH;
+        auto kernel =
+            vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit> : sgemm_ffma_tma_kernel<T, false, sgemm::kRoleSplit>;
+        // behind a plain grid of the same product: start on the SMs it frees as it drains
+        const bool overlap = tile_base > 0 && !(dbg & kDebugNoOverlap);
+        cudaLaunchAttribute attr[2];
+        const cudaLaunchConfig_t cfg = split_config<T>(tiles, cs, overlap, stream, attr);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc,
+                                                 (float *)nullptr, 0, (int)tile_base, info.err_word, wait, dbg);
+        return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
 }
 
 // Launch the product kernel over a (tiles x splits) grid.  splits > 1 writes
@@ -172,9 +324,23 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     // partial slabs hold the raw products; alpha and beta act in the reduction
     const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
     if (use_tma(p)) {
-        if (splits == 1 && p.K <= 2 * TmaSmallK::BK)
-            return launch_tma<TmaSmallK>(p, alpha, beta, vc, splits, partials, ldp, stream, info);
-        return launch_tma<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, stream, info);
+        if (splits == 1 && p.K <= 2 * TmaSmallK::BK) {
+            const int64_t tiles =
+                (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
+            return launch_tma<TmaSmallK>(p, alpha, beta, vc, 1, partials, ldp, 0, tiles, 1, false, stream, info);
+        }
+        if (splits == 1) {
+            const SplitPlan plan = split_plan(p.M, p.N, p.K, info);
+            if (plan.full > 0) {
+                const int st =
+                    launch_tma<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.full, 1, plan.cs > 1, stream, info);
+                if (st != SGEMM_OK || plan.full == plan.tiles) return st;
+            }
+            return launch_tma<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, plan.full, plan.tiles - plan.full,
+                                       plan.cs, false, stream, info);
+        }
+        const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
+        return launch_tma<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, 0, tiles, 1, false, stream, info);
     } else {
         using T = CpTile;
         const bool vb = aligned16(p.B) && p.ldb % 4 == 0;
@@ -350,6 +516,25 @@ int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int 
     DeviceInfo info;
     if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
     return launch_product(p, 1, nullptr, 0, stream, info);
+}
+
+int sgemm_f32_plan(int M, int N, int K, long long *tiles, long long *full_tiles, int *cluster_size) {
+    if (!tiles || !full_tiles || !cluster_size || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    *tiles = *full_tiles = 0;
+    *cluster_size = 1;
+    if ((int64_t)M * N == 0) return SGEMM_OK;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    if (K <= 2 * TmaSmallK::BK) {
+        *tiles = *full_tiles =
+            (long long)((M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((N + TmaSmallK::BN - 1) / TmaSmallK::BN);
+        return SGEMM_OK;
+    }
+    const SplitPlan plan = split_plan(M, N, K, info);
+    *tiles = plan.tiles;
+    *full_tiles = plan.full;
+    *cluster_size = plan.cs;
+    return SGEMM_OK;
 }
 
 size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits) { return partials_bytes(M, N, splits); }
@@ -577,9 +762,15 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
 
 namespace {
 
+// B is copied in up to kHostBChunks column blocks so that the first row panel's
+// products can start on the first block instead of waiting for all of B.
+constexpr int kHostBChunks = 8;
+
 struct HostPlan {
     int rows;          // rows of C per panel (a multiple of the 128-row tile)
     int panels;
+    int chunks;        // column blocks of B (whole 128-column tiles each)
+    int chunk_cols;    // columns per block (the last one may be narrower)
     int64_t lda_d;     // device row pitch of the A panels (floats)
     int64_t ldn_d;     // device row pitch of B and of the C panels
     size_t b_bytes, a_bytes, c_bytes, total;
@@ -609,6 +800,15 @@ HostPlan host_plan(int M, int N, int K, int panels, int sms) {
     if (rows < 1) rows = 1;
     h.rows = (int)rows;
     h.panels = (int)((M + rows - 1) / rows);
+    // column blocks of B for the first panel: at most kHostBChunks, each wide
+    // enough that the first panel's product over it still gives every SM a tile
+    const int64_t tiles_m0 = (rows + TmaTile::BM - 1) / TmaTile::BM;
+    int64_t per = (tiles_n + kHostBChunks - 1) / kHostBChunks;
+    const int64_t fill = ((int64_t)(sms > 0 ? sms : 1) + tiles_m0 - 1) / tiles_m0;
+    if (per < fill) per = fill;
+    if (per > tiles_n) per = tiles_n > 0 ? tiles_n : 1;
+    h.chunk_cols = (int)(per * TmaTile::BN);
+    h.chunks = (int)((N + h.chunk_cols - 1) / h.chunk_cols);
     h.lda_d = ld4(K);
     h.ldn_d = ld4(N);
     h.b_bytes = (size_t)K * h.ldn_d * sizeof(float);
@@ -656,15 +856,20 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
     float *dC[2] = {reinterpret_cast<float *>(base + up(h.b_bytes) + 2 * up(h.a_bytes)),
                     reinterpret_cast<float *>(base + up(h.b_bytes) + 2 * up(h.a_bytes) + up(h.c_bytes))};
 
-    // events: call start; B landed; A panel landed; A panel consumed; C panel
-    // ready; C panel copied out
-    cudaEvent_t ev_start, ev_b, ev_a[2], ev_a_free[2], ev_c[2], ev_c_free[2];
-    cudaEvent_t *all[] = {&ev_start, &ev_b, &ev_a[0], &ev_a[1], &ev_a_free[0], &ev_a_free[1],
-                          &ev_c[0], &ev_c[1], &ev_c_free[0], &ev_c_free[1]};
+    // events: call start; each column block of B landed; A panel landed; A
+    // panel consumed; C panel ready; C panel copied out
+    cudaEvent_t ev_start, ev_b[kHostBChunks], ev_a[2], ev_a_free[2], ev_c[2], ev_c_free[2];
+    cudaEvent_t *all[1 + kHostBChunks + 8];
+    int n_ev = 0;
+    all[n_ev++] = &ev_start;
+    for (int j = 0; j < h.chunks; ++j) all[n_ev++] = &ev_b[j];
+    for (cudaEvent_t *e : {&ev_a[0], &ev_a[1], &ev_a_free[0], &ev_a_free[1], &ev_c[0], &ev_c[1], &ev_c_free[0],
+                           &ev_c_free[1]})
+        all[n_ev++] = e;
     int made = 0;
     int st = SGEMM_OK;
-    for (cudaEvent_t *e : all) {
-        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+    for (int i = 0; i < n_ev; ++i) {
+        if (cudaEventCreateWithFlags(all[i], cudaEventDisableTiming) != cudaSuccess) {
             st = SGEMM_ERR_LAUNCH;
             break;
         }
@@ -680,12 +885,10 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
         ok(cudaEventRecord(ev_start, stream));
         ok(cudaStreamWaitEvent(h2d_stream, ev_start, 0));
         ok(cudaStreamWaitEvent(d2h_stream, ev_start, 0));
-        ok(cudaMemcpy2DAsync(dB, h.ldn_d * sizeof(float), B, (size_t)ldb * sizeof(float), (size_t)N * sizeof(float),
-                             K, cudaMemcpyHostToDevice, h2d_stream));
-        ok(cudaEventRecord(ev_b, h2d_stream));
-        ok(cudaStreamWaitEvent(stream, ev_b, 0));
     }
-    for (int p = 0; p < h.panels && st == SGEMM_OK; ++p) {
+    // the first A panel, then B in column blocks (the first panel's products
+    // follow the blocks as they land), then the other A panels
+    auto copy_a = [&](int p) {
         const int b = p & 1;
         const int r0 = p * h.rows;
         const int rows = (M - r0) < h.rows ? (M - r0) : h.rows;
@@ -694,16 +897,37 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
         ok(cudaMemcpy2DAsync(dA[b], h.lda_d * sizeof(float), A + (int64_t)r0 * lda, (size_t)lda * sizeof(float),
                              (size_t)K * sizeof(float), rows, cudaMemcpyHostToDevice, h2d_stream));
         ok(cudaEventRecord(ev_a[b], h2d_stream));
+    };
+    if (st == SGEMM_OK) copy_a(0);
+    for (int j = 0; j < h.chunks && st == SGEMM_OK; ++j) {
+        const int c0 = j * h.chunk_cols;
+        const int cols = (N - c0) < h.chunk_cols ? (N - c0) : h.chunk_cols;
+        ok(cudaMemcpy2DAsync(dB + c0, h.ldn_d * sizeof(float), B + c0, (size_t)ldb * sizeof(float),
+                             (size_t)cols * sizeof(float), K, cudaMemcpyHostToDevice, h2d_stream));
+        ok(cudaEventRecord(ev_b[j], h2d_stream));
+    }
+    for (int p = 0; p < h.panels && st == SGEMM_OK; ++p) {
+        const int b = p & 1;
+        const int r0 = p * h.rows;
+        const int rows = (M - r0) < h.rows ? (M - r0) : h.rows;
+        if (p >= 1) copy_a(p);
         // the product, once its A panel has landed and its C buffer has been copied out
         ok(cudaStreamWaitEvent(stream, ev_a[b], 0));
         if (p >= 2) ok(cudaStreamWaitEvent(stream, ev_c_free[b], 0));
         if (st != SGEMM_OK) break;
-        const Problem prob{rows, N, K, dA[b], (int)h.lda_d, dB, (int)h.ldn_d, dC[b], (int)h.ldn_d};
-        const int ls = launch_product(prob, 1, nullptr, 0, stream, info);
-        if (ls != SGEMM_OK) {
-            st = ls;
-            break;
+        // panel 0: one product per column block of B, each once its block has
+        // landed; later panels: one product over all of B (every block has landed)
+        const int parts = p == 0 ? h.chunks : 1;
+        for (int j = 0; j < parts && st == SGEMM_OK; ++j) {
+            const int c0 = p == 0 ? j * h.chunk_cols : 0;
+            const int cols = p == 0 ? ((N - c0) < h.chunk_cols ? (N - c0) : h.chunk_cols) : N;
+            if (p == 0) ok(cudaStreamWaitEvent(stream, ev_b[j], 0));
+            if (st != SGEMM_OK) break;
+            const Problem prob{rows, cols, K, dA[b], (int)h.lda_d, dB + c0, (int)h.ldn_d, dC[b] + c0, (int)h.ldn_d};
+            const int ls = launch_product(prob, 1, nullptr, 0, stream, info);
+            if (ls != SGEMM_OK) st = ls;
         }
+        if (st != SGEMM_OK) break;
         ok(cudaEventRecord(ev_a_free[b], stream));
         ok(cudaEventRecord(ev_c[b], stream));
         // copy the C panel back to the host rows

@@ -65,6 +65,12 @@ typedef enum {
  *     per thread accumulated with packed two-wide FP32 FMAs;
  *   - otherwise: 128 x 128 block tiles copied by cp.async with per-element
  *     masks, 8 x 8 outputs per thread.
+ * On the TMA path, when a grid would leave SMs idle (few tiles, or a last
+ * partial round of tiles over the SMs), those tiles are each shared by a
+ * thread-block cluster of 2, 4 or 8 blocks that split its k-steps and add their
+ * partial sums through distributed shared memory in a fixed rank order: no
+ * workspace, and the same bits on every run (sgemm_f32_plan reports the
+ * choice).
  * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
  * The TMA kernel's waits are bounded: if a copy never lands, its blocks give
  * up, write nothing, and the next sgemm_device_status() returns
@@ -75,6 +81,18 @@ int sgemm_f32(int M, int N, int K,
               const float *B, int ldb,
               float *C, int ldc,
               cudaStream_t stream);
+
+/*
+ * How sgemm_f32 launches an M x N x K product with aligned operands (the TMA
+ * path, K > 64) on the current device: *tiles = the number of 128 x 128 output
+ * tiles; the first *full_tiles of them run as a plain grid, the rest as
+ * clusters of *cluster_size blocks that split each tile's k-steps
+ * (*cluster_size == 1: no cluster split, *full_tiles == *tiles).  The result
+ * reflects the test-only switches of sgemm_debug_set.  Launches nothing.
+ * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
+ * if the device cannot be queried.
+ */
+int sgemm_f32_plan(int M, int N, int K, long long *tiles, long long *full_tiles, int *cluster_size);
 
 /*
  * Split-K form of sgemm_f32 for grids with fewer output tiles than the GPU has
@@ -219,13 +237,17 @@ size_t sgemm_gemm_workspace_size(int algo, int transa, int transb, int M, int N,
 
 /*
  * C = A * B with A, B and C in HOST memory: the end-to-end form of sgemm_f32.
- * B is copied to the device once; then, panel by panel of at most `panels`
- * row panels of C (each rounded up to whole waves of 128 x 128 output tiles
- * on this device, so fewer panels may result), the rows of A are copied in
- * on h2d_stream, the product runs on `stream` with the kernels of sgemm_f32,
- * and the rows of C are copied back on d2h_stream, so that copies of one panel
- * overlap the product of another.  Every element of C is computed exactly as
- * sgemm_f32 computes it.
+ * B is copied to the device once, in up to 8 column blocks; then, panel by
+ * panel of at most `panels` row panels of C (each rounded up to whole waves of
+ * 128 x 128 output tiles on this device, so fewer panels may result), the rows
+ * of A are copied in on h2d_stream, the product runs on `stream` with the
+ * kernels of sgemm_f32, and the rows of C are copied back on d2h_stream, so
+ * that copies of one panel overlap the product of another.  The first panel's
+ * product runs block by block as the blocks of B land.  Each product is an
+ * sgemm_f32 launch on the device copies: every element is held to the same
+ * bound, and its bits equal sgemm_f32's on the whole product except where the
+ * cluster split divides that element's k-steps differently for a panel than
+ * for the whole (never when neither splits).
  *   workspace: caller-owned device memory of at least
  *     sgemm_f32_host_workspace_size(M, N, K, panels) bytes (B, two A panels
  *     and two C panels), 16-byte aligned; the library allocates nothing.
@@ -296,7 +318,12 @@ int sgemm_device_status(cudaStream_t stream);
  * TEST-ONLY.  flags bit 0: the TMA-fed kernels never issue their copies, so every
  * block's bounded wait runs out (used to check the timeout path without any
  * fault); bit 1: route every product to the cp.async kernel, so both kernels
- * can be checked on the same inputs.  wait_limit_ns: the bound of each wait
+ * can be checked on the same inputs; bits 4..7: the cluster size of the TMA
+ * path's cluster split, forced (0 = automatic, 1 = never split, 2 .. 8 =
+ * split the tiles beyond whole multiples of the SM count with that size);
+ * bit 8: with a forced size, split every tile; bit 9: no programmatic overlap
+ * of the cluster-split launch with the plain one before it.  wait_limit_ns:
+ * the bound of each wait
  * (default 2 s).  Affects every
  * later launch in this process.  SGEMM_ERR_INVALID_ARG if flags < 0 or
  * wait_limit_ns == 0.

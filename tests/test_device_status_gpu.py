@@ -28,19 +28,20 @@ def test_status_ok_after_normal_products(sg):
     assert sg.sgemm_device_status() == sg.SGEMM_OK
 
 
-def test_timeout_is_reported_and_nothing_is_written(sg):
+@pytest.mark.parametrize("K", [64, 96])   # the small-K tile and the main tile
+def test_timeout_is_reported_and_nothing_is_written(sg, K):
     import torch
-    A, B = gen.operands(128, 256, 64, seed=31)
+    A, B = gen.operands(128, 256, K, seed=31)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((128, 256), CANARY_BITS, np.int32).view(np.float32)).cuda()
     sg.sgemm_debug_set(1, 50_000_000)     # copies never issued; 50 ms bound per wait
-    sg.sgemm_f32(128, 256, 64, dA, 64, dB, 256, dC, 256)
+    sg.sgemm_f32(128, 256, K, dA, K, dB, 256, dC, 256)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
     # the status is cleared by reading it
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     # and the device is still usable
     sg.sgemm_debug_set(0, 2_000_000_000)
-    sg.sgemm_f32(128, 256, 64, dA, 64, dB, 256, dC, 256)
+    sg.sgemm_f32(128, 256, K, dA, K, dB, 256, dC, 256)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)

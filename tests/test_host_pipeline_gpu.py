@@ -1,6 +1,8 @@
 """sgemm_f32_host: host-memory operands, copies overlapped with the product
-over row panels.  Every element must equal sgemm_f32's (same kernels, same
-per-element arithmetic), for any panel count, ragged shapes and strides."""
+over row panels (the first panel's product block by block over the column
+blocks of B).  Within the oracle's bound for any panel count, ragged shapes and
+strides; and equal bit for bit to sgemm_f32 when the cluster split is off on
+both sides (same kernels, same per-element arithmetic)."""
 
 import numpy as np
 import pytest
@@ -44,12 +46,37 @@ def device_product(sg, A, B):
     return C.cpu().numpy()
 
 
+NO_SPLIT = 1 << 4
+
+
 @pytest.mark.parametrize("panels", [1, 2, 3, 8])
 def test_equals_sgemm_f32(sg, panels):
     A, B = gen.operands(1000, 520, 300, seed=120)
-    C = host_product(sg, A, B, panels)
-    assert np.array_equal(C, device_product(sg, A, B))
-    check_full(C, A, B)
+    check_full(host_product(sg, A, B, panels), A, B)
+    sg.sgemm_debug_set(NO_SPLIT)
+    try:
+        C = host_product(sg, A, B, panels)
+        assert np.array_equal(C, device_product(sg, A, B))
+    finally:
+        sg.sgemm_debug_set(0)
+
+
+def test_several_panels_and_column_blocks(sg):
+    # enough rows for several wave-rounded panels; N spans 8 column blocks of B
+    # with a ragged last block
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K = 128 * sms * 2 + 77, 128 * 17 + 40, 160
+    A, B = gen.operands(M, N, K, seed=123)
+    C = host_product(sg, A, B, 3)
+    rows = [0, 1, 127, 128, M // 2, M - 78, M - 77, M - 1] + list(np.random.default_rng(2).integers(0, M, 10))
+    from helpers import check_rows
+    check_rows(C, A, B, rows)
+    sg.sgemm_debug_set(NO_SPLIT)
+    try:
+        assert np.array_equal(host_product(sg, A, B, 3), device_product(sg, A, B))
+    finally:
+        sg.sgemm_debug_set(0)
 
 
 def test_strides_and_ragged(sg):
@@ -94,4 +121,4 @@ def test_back_to_back_calls_share_a_workspace(sg):
         hosts.append((hA, hB, hC))
     s0.synchronize()
     for (A, B), (_, _, hC) in zip(pairs, hosts):
-        assert np.array_equal(hC.numpy(), device_product(sg, A, B))
+        check_full(hC.numpy(), A, B)

@@ -17,11 +17,13 @@ def sg(cuda_device, lib):
     return sg
 
 
-@pytest.fixture(params=["auto", "cp.async"])
+@pytest.fixture(params=["auto", "no-cluster-split", "cp.async"])
 def path(request, sg):
-    """Run the test with the library's own kernel choice, and again with every
-    product routed to the cp.async kernel (test-only switch)."""
-    sg.sgemm_debug_set(2 if request.param == "cp.async" else 0, 2_000_000_000)
+    """Run the test with the library's own kernel choice, again with the TMA
+    path's cluster split switched off, and again with every product routed to
+    the cp.async kernel (test-only switches)."""
+    flags = {"auto": 0, "no-cluster-split": 1 << 4, "cp.async": 2}[request.param]
+    sg.sgemm_debug_set(flags, 2_000_000_000)
     yield request.param
     sg.sgemm_debug_set(0, 2_000_000_000)
 
