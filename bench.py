@@ -253,7 +253,7 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
             sg.sgemm_gemm(0, 0, 0, M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, ws, ws_bytes, handle)
         # the product runs on 16-byte aligned (repacked if need be) operands: the
         # TMA path's one or two launches; the repacking copies are not kernels of ours
-        return step, f32_launches(sg, M, N, K, aligned=True)
+        return step, f32_launches(sg, M, N, K)
     if path in LADDER:
         cfg["path"] = path
 
@@ -274,10 +274,10 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
     return step, f32_launches(sg, M, N, K)
 
 
-def f32_launches(sg, M, N, K, aligned=False):
-    """Kernels one sgemm_f32 call launches for contiguous operands: one, or two
-    when a cluster-split grid follows whole rounds of plain tiles."""
-    if K > 64 and (aligned or (K % 4 == 0 and N % 4 == 0)):
+def f32_launches(sg, M, N, K):
+    """Kernels one sgemm_f32 call launches: one, or two when a cluster-split
+    grid follows whole rounds of plain tiles (sgemm_f32_plan)."""
+    if K > 0 and M * N > 0:
         tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
         return 2 if cs > 1 and 0 < full < tiles else 1
     return 1
@@ -318,7 +318,13 @@ def kernel_name(sg, M, N, K):
             name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                      "added through distributed shared memory)")
         return name
-    return "sgemm_ffma_kernel (128x128x16 cp.async tile, 4 stages, 8x8 per thread)"
+    name = ("sgemm_ffma_cp_kernel (128x128x32 tile fed by cp.async, 3 stages, 8x16 per thread as fma.rn.f32x2 "
+            "column pairs, 2 CTAs/SM)")
+    tiles, full, cs = sg.sgemm_f32_plan(M, N, K) if K > 64 else (0, 0, 1)
+    if cs > 1:
+        name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
+                 "added through distributed shared memory)")
+    return name
 
 
 def max_over_ranks(value, world, device):

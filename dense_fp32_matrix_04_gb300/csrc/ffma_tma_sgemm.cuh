@@ -113,6 +113,182 @@ enum : int { kDeviceErrNone = 0, kDeviceErrTimeout = 1 };
 // bounded waits run out.
 enum : int { kDebugSkipCopies = 1 };
 
+// One pipeline stage of the outer-product FMAs: BK k-values for this thread's
+// TM x TN block of C, reading its A rows at `sa` (128-byte rows with the
+// 128-byte swizzle: the thread's rows are lm + 8 i) and its B row segments at
+// `sb`.
+template <class T>
+__device__ __forceinline__ void tile_fma(float (&acc)[T::PACKED ? 1 : T::TM][T::PACKED ? 1 : T::TN],
+                                         uint64_t (&acc2)[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1],
+                                         const unsigned char *sa, const unsigned char *sb, int lm) {
+#pragma unroll T::G_UNROLL
+    for (int g = 0; g < T::BK / 4; ++g) {
+        // four k-values for each of the 8 rows, from the swizzled chunk g ^ lm
+        const unsigned char *ag = sa + ((g ^ lm) << 4);
+        float4 a[T::TM];
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i) a[i] = *reinterpret_cast<const float4 *>(ag + 1024 * i);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const unsigned char *bk = sb + (4 * g + kk) * (T::BN * 4);
+            if constexpr (T::PACKED) {
+                uint64_t b2[T::TN / 2];
+#pragma unroll
+                for (int q = 0; q < T::TN / 4; ++q) {
+                    const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(bk + 64 * q);
+                    b2[2 * q] = v.x;
+                    b2[2 * q + 1] = v.y;
+                }
+                if (T::ORDER == 1) {
+                    // column-pair outer: one B pair reused down the TM rows
+                    uint64_t ad[T::TM];
+#pragma unroll
+                    for (int i = 0; i < T::TM; ++i)
+                        ad[i] = f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
+#pragma unroll
+                    for (int j = 0; j < T::TN / 2; ++j)
+#pragma unroll
+                        for (int i = 0; i < T::TM; ++i) f32x2_fma(acc2[i][j], ad[i], b2[j]);
+                } else {
+                    // row outer: one duplicated A value reused across the row of pairs
+#pragma unroll
+                    for (int i = 0; i < T::TM; ++i) {
+                        const uint64_t ad =
+                            f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
+#pragma unroll
+                        for (int j = 0; j < T::TN / 2; ++j) f32x2_fma(acc2[i][j], ad, b2[j]);
+                    }
+                }
+            } else {
+            float b[T::TN];
+#pragma unroll
+            for (int q = 0; q < T::TN / 4; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(bk + 64 * q);
+                b[4 * q + 0] = v.x;
+                b[4 * q + 1] = v.y;
+                b[4 * q + 2] = v.z;
+                b[4 * q + 3] = v.w;
+            }
+            float av[T::TM];
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i)
+                av[i] = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+            if (T::ORDER == 1) {
+#pragma unroll
+                for (int j = 0; j < T::TN; ++j)
+#pragma unroll
+                    for (int i = 0; i < T::TM; ++i) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+            } else if (T::ORDER == 2) {
+#pragma unroll
+                for (int i = 0; i < T::TM; i += 2)
+#pragma unroll
+                    for (int j = 0; j < T::TN; ++j) {
+                        acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+                        acc[i + 1][j] = fmaf(av[i + 1], b[j], acc[i + 1][j]);
+                    }
+            } else {
+#pragma unroll
+                for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < T::TN; ++j) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
+            }
+            }  // scalar form
+        }
+    }
+}
+
+// The cluster split's exchange, after the k-loop of every CTA of a cluster of
+// cs: each parks its packed partial sums in its own stage buffers (which every
+// warp has finished reading), with a flag word saying whether it gave up on a
+// wait; after a cluster barrier, rank r adds up its share of the rows -- rows
+// i of each thread with i * cs / TM == r -- over ranks 0, 1, ..., cs - 1 in
+// that order, reading the other ranks' shared memory; a second barrier keeps
+// every CTA's shared memory in place until all ranks have read it.  Returns
+// true when some rank gave up (then nothing may be stored).  Every thread of
+// every CTA of the cluster must call it.
+template <class T>
+__device__ __forceinline__ bool cluster_reduce(uint64_t (&acc2)[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1],
+                                               uint32_t base, unsigned char *smem, int tid, int cs, int rank,
+                                               bool failed) {
+    // 16-byte chunk c = i * TN/4 + q (accumulator pairs 2q, 2q + 1 of row i) of
+    // thread tid sits at (c * THREADS + tid) * 16; the flag word follows the chunks
+    constexpr int CHUNKS = T::TM * T::TN / 4;
+    const uint32_t flag = base + CHUNKS * T::THREADS * 16;
+    if (!failed) {
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+            for (int q = 0; q < T::TN / 4; ++q)
+                *reinterpret_cast<ulonglong2 *>(smem + ((i * (T::TN / 4) + q) * T::THREADS + tid) * 16) =
+                    make_ulonglong2(acc2[i][2 * q], acc2[i][2 * q + 1]);
+    }
+    if (tid == 0) *reinterpret_cast<volatile uint32_t *>(smem + CHUNKS * T::THREADS * 16) = failed;
+    cluster_sync();
+    uint32_t bad = 0;
+    for (int r = 0; r < cs; ++r) bad |= dsmem_ld_u32(dsmem_map(flag, (uint32_t)r));
+    if (!bad) {
+        const uint64_t one2 = f32x2_dup(1.f);
+#pragma unroll
+        for (int i = 0; i < T::TM; ++i) {
+            if ((i * cs) / T::TM != rank) continue;
+#pragma unroll
+            for (int q = 0; q < T::TN / 4; ++q) {
+                const uint32_t off = base + ((i * (T::TN / 4) + q) * T::THREADS + tid) * 16;
+                uint64_t s0 = acc2[i][2 * q], s1 = acc2[i][2 * q + 1];
+                if (rank != 0) {
+                    const ulonglong2 v = dsmem_ld_v2u64(dsmem_map(off, 0));
+                    s0 = v.x;
+                    s1 = v.y;
+                }
+                for (int r = 1; r < cs; ++r) {
+                    uint64_t v0 = acc2[i][2 * q], v1 = acc2[i][2 * q + 1];
+                    if (r != rank) {
+                        const ulonglong2 v = dsmem_ld_v2u64(dsmem_map(off, (uint32_t)r));
+                        v0 = v.x;
+                        v1 = v.y;
+                    }
+                    f32x2_fma(s0, v0, one2);  // s + v, rounded once (v * 1 is exact)
+                    f32x2_fma(s1, v1, one2);
+                }
+                acc2[i][2 * q] = s0;
+                acc2[i][2 * q + 1] = s1;
+            }
+        }
+    }
+    cluster_sync();
+    return bad != 0;
+}
+
+// Epilogue: this thread's rows r0 + 8 i and 16-byte column quads at c0 + 16 q
+// (matrix coordinates); C = alpha * acc + beta * C, masked at the edges.  With
+// the cluster split, only the rows this rank added up.
+template <class T, bool VEC_C, bool CSPLIT>
+__device__ __forceinline__ void store_tile(const float (&acc)[T::PACKED ? 1 : T::TM][T::PACKED ? 1 : T::TN],
+                                           const uint64_t (&acc2)[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1],
+                                           float *C, int ldc, int M, int N, int r0, int c0, float alpha, float beta,
+                                           int cs, int rank) {
+#pragma unroll
+    for (int i = 0; i < T::TM; ++i) {
+        const int row = r0 + 8 * i;
+        if (row >= M) continue;
+        if (CSPLIT && (i * cs) / T::TM != rank) continue;
+        float *crow = C + (int64_t)row * ldc;
+#pragma unroll
+        for (int q = 0; q < T::TN / 4; ++q) {
+            const int col = c0 + 16 * q;
+            float vp[4];
+            if constexpr (T::PACKED) {
+                const float2 lo = f32x2_unpack(acc2[i][2 * q]), hi = f32x2_unpack(acc2[i][2 * q + 1]);
+                vp[0] = lo.x, vp[1] = lo.y, vp[2] = hi.x, vp[3] = hi.y;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) vp[j] = acc[i][4 * q + j];
+            }
+            store_quad<VEC_C>(crow, col, N, vp, alpha, beta);
+        }
+    }
+}
+
 // What a launch of the kernel does: a plain grid of tiles; the same, as the
 // first of a plain + cluster-split pair (it lets the second grid start early);
 // or the cluster-split grid.
@@ -217,80 +393,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         if (ok) {
             const unsigned char *sa = smem + s * T::STAGE + row0 * 128;
             const unsigned char *sb = smem + s * T::STAGE + T::A_STAGE + col0 * 4;
-#pragma unroll T::G_UNROLL
-            for (int g = 0; g < T::BK / 4; ++g) {
-                // four k-values for each of the 8 rows, from the swizzled chunk g ^ lm
-                const unsigned char *ag = sa + ((g ^ lm) << 4);
-                float4 a[T::TM];
-#pragma unroll
-                for (int i = 0; i < T::TM; ++i) a[i] = *reinterpret_cast<const float4 *>(ag + 1024 * i);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const unsigned char *bk = sb + (4 * g + kk) * (T::BN * 4);
-                    if constexpr (T::PACKED) {
-                        uint64_t b2[T::TN / 2];
-#pragma unroll
-                        for (int q = 0; q < T::TN / 4; ++q) {
-                            const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(bk + 64 * q);
-                            b2[2 * q] = v.x;
-                            b2[2 * q + 1] = v.y;
-                        }
-                        if (T::ORDER == 1) {
-                            // column-pair outer: one B pair reused down the TM rows
-                            uint64_t ad[T::TM];
-#pragma unroll
-                            for (int i = 0; i < T::TM; ++i)
-                                ad[i] = f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
-#pragma unroll
-                            for (int j = 0; j < T::TN / 2; ++j)
-#pragma unroll
-                                for (int i = 0; i < T::TM; ++i) f32x2_fma(acc2[i][j], ad[i], b2[j]);
-                        } else {
-                            // row outer: one duplicated A value reused across the row of pairs
-#pragma unroll
-                            for (int i = 0; i < T::TM; ++i) {
-                                const uint64_t ad =
-                                    f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
-#pragma unroll
-                                for (int j = 0; j < T::TN / 2; ++j) f32x2_fma(acc2[i][j], ad, b2[j]);
-                            }
-                        }
-                    } else {
-                    float b[T::TN];
-#pragma unroll
-                    for (int q = 0; q < T::TN / 4; ++q) {
-                        const float4 v = *reinterpret_cast<const float4 *>(bk + 64 * q);
-                        b[4 * q + 0] = v.x;
-                        b[4 * q + 1] = v.y;
-                        b[4 * q + 2] = v.z;
-                        b[4 * q + 3] = v.w;
-                    }
-                    float av[T::TM];
-#pragma unroll
-                    for (int i = 0; i < T::TM; ++i)
-                        av[i] = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-                    if (T::ORDER == 1) {
-#pragma unroll
-                        for (int j = 0; j < T::TN; ++j)
-#pragma unroll
-                            for (int i = 0; i < T::TM; ++i) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
-                    } else if (T::ORDER == 2) {
-#pragma unroll
-                        for (int i = 0; i < T::TM; i += 2)
-#pragma unroll
-                            for (int j = 0; j < T::TN; ++j) {
-                                acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
-                                acc[i + 1][j] = fmaf(av[i + 1], b[j], acc[i + 1][j]);
-                            }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < T::TM; ++i)
-#pragma unroll
-                            for (int j = 0; j < T::TN; ++j) acc[i][j] = fmaf(av[i], b[j], acc[i][j]);
-                    }
-                    }  // scalar form
-                }
-            }
+            tile_fma<T>(acc, acc2, sa, sb, lm);
         }
         // every warp is done with stage s (or the CTA gives up together)
         if (__syncthreads_or(!ok)) {
@@ -315,85 +418,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     }
 
     if constexpr (CSPLIT) {
-        // 16-byte chunk c = i * TN/4 + q (accumulator pairs 2q, 2q + 1 of row i) of
-        // thread tid sits at (c * THREADS + tid) * 16 in the stage buffers, which
-        // every warp has finished reading (the loop's last barrier); a word after
-        // the chunks says whether this CTA gave up on a wait
-        constexpr int CHUNKS = T::TM * T::TN / 4;
-        const uint32_t flag = base + CHUNKS * T::THREADS * 16;
-        if (failed_kt < 0) {
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i)
-#pragma unroll
-                for (int q = 0; q < T::TN / 4; ++q)
-                    *reinterpret_cast<ulonglong2 *>(smem + ((i * (T::TN / 4) + q) * T::THREADS + tid) * 16) =
-                        make_ulonglong2(acc2[i][2 * q], acc2[i][2 * q + 1]);
-        }
-        if (tid == 0) *reinterpret_cast<volatile uint32_t *>(smem + CHUNKS * T::THREADS * 16) = failed_kt >= 0;
-        cluster_sync();
-        uint32_t bad = 0;
-        for (int r = 0; r < cs; ++r) bad |= dsmem_ld_u32(dsmem_map(flag, (uint32_t)r));
-        if (!bad) {
-            const uint64_t one2 = f32x2_dup(1.f);
-            // rows i with i * cs / TM == rank are this CTA's share (cs <= TM): the sum over
-            // ranks 0, 1, ..., cs - 1 in that order, whichever CTA computes it
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i) {
-                if ((i * cs) / T::TM != rank) continue;
-#pragma unroll
-                for (int q = 0; q < T::TN / 4; ++q) {
-                    const uint32_t off = base + ((i * (T::TN / 4) + q) * T::THREADS + tid) * 16;
-                    uint64_t s0 = acc2[i][2 * q], s1 = acc2[i][2 * q + 1];
-                    if (rank != 0) {
-                        const ulonglong2 v = dsmem_ld_v2u64(dsmem_map(off, 0));
-                        s0 = v.x;
-                        s1 = v.y;
-                    }
-                    for (int r = 1; r < cs; ++r) {
-                        uint64_t v0 = acc2[i][2 * q], v1 = acc2[i][2 * q + 1];
-                        if (r != rank) {
-                            const ulonglong2 v = dsmem_ld_v2u64(dsmem_map(off, (uint32_t)r));
-                            v0 = v.x;
-                            v1 = v.y;
-                        }
-                        f32x2_fma(s0, v0, one2);  // s + v, rounded once (v * 1 is exact)
-                        f32x2_fma(s1, v1, one2);
-                    }
-                    acc2[i][2 * q] = s0;
-                    acc2[i][2 * q + 1] = s1;
-                }
-            }
-        }
-        // the other CTAs' shared memory must stay in place until every rank has read it
-        cluster_sync();
-        if (bad) {
+        if (cluster_reduce<T>(acc2, base, smem, tid, cs, rank, failed_kt >= 0)) {
             griddep_wait();
             return;
         }
     }
-
-    // epilogue: rows row0 + 8 i, 16-byte column quads at col0 + 16 q;
-    // C = alpha * acc + beta * C (partial slabs are written with alpha = 1, beta = 0)
-#pragma unroll
-    for (int i = 0; i < T::TM; ++i) {
-        const int row = m0 + row0 + 8 * i;
-        if (row >= M) continue;
-        if (CSPLIT && (i * cs) / T::TM != rank) continue;
-        float *crow = C + (int64_t)row * ldc;
-#pragma unroll
-        for (int q = 0; q < T::TN / 4; ++q) {
-            const int col = n0 + col0 + 16 * q;
-            float vp[4];
-            if constexpr (T::PACKED) {
-                const float2 lo = f32x2_unpack(acc2[i][2 * q]), hi = f32x2_unpack(acc2[i][2 * q + 1]);
-                vp[0] = lo.x, vp[1] = lo.y, vp[2] = hi.x, vp[3] = hi.y;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) vp[j] = acc[i][4 * q + j];
-            }
-            store_quad<VEC_C>(crow, col, N, vp, alpha, beta);
-        }
-    }
+    store_tile<T, VEC_C, CSPLIT>(acc, acc2, C, ldc, M, N, m0 + row0, n0 + col0, alpha, beta, cs, rank);
     // a cluster-split grid overlapping a plain one completes after it
     if constexpr (CSPLIT) griddep_wait();
 }

@@ -10,7 +10,7 @@
 #include <mutex>
 
 #include "../../include/sgemm.h"
-#include "ffma_sgemm.cuh"
+#include "ffma_cp_packed.cuh"
 #include "ffma_tma_sgemm.cuh"
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
@@ -29,8 +29,6 @@ static __device__ __align__(256) float g_splitk_noalloc_scratch[kNoallocScratchF
 
 namespace {
 
-// 128 x 128 CTA tile, 16-deep k-steps, 4 cp.async stages, 2 CTAs per SM.
-using CpTile = sgemm::FfmaTile<128, 128, 16, 4, 2>;
 using TmaTile = sgemm::TmaMainTile;
 using TmaSmallK = sgemm::TmaSmallKTile;
 using X3Tile = sgemm::Tf32x3MainTile;
@@ -139,21 +137,12 @@ bool use_tma(const Problem &p) {
            !(g_debug_flags.load() & kDebugForceCpAsync);
 }
 
-int k_tiles(const Problem &p) {
-    const int bk = use_tma(p) ? TmaTile::BK : CpTile::BK;
-    return (p.K + bk - 1) / bk;
-}
+int k_tiles(const Problem &p) { return (p.K + TmaTile::BK - 1) / TmaTile::BK; }
 
 template <class T, bool VC, int ROLE>
 bool tma_attr(int dev) {
     static std::atomic<int> done[kMaxDevices];
     return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC, ROLE>, T::SMEM_BYTES);
-}
-
-template <class T, bool VB, bool VC>
-bool cp_attr(int dev) {
-    static std::atomic<int> done[kMaxDevices];
-    return smem_attr_once(done[dev], sgemm::sgemm_ffma_kernel<T, VB, VC>, T::SMEM_BYTES);
 }
 
 // The cluster-split launch configuration: `clusters` clusters of cs CTAs and,
@@ -316,6 +305,53 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
     }
 }
 
+template <class T, bool VA, bool VB, int ROLE>
+bool cp_packed_attr(int dev) {
+    static std::atomic<int> done[kMaxDevices];
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_cp_kernel<T, VA, VB, ROLE>, T::SMEM_BYTES);
+}
+
+// The packed cp.async kernel for the given operand alignment and launch role.
+template <class T, int ROLE>
+bool cp_packed_kernel(bool va, bool vb, int dev,
+                      void (*&kernel)(int, int, int, float, const float *, int, const float *, int, float, float *, int,
+                                      int, float *, int, int)) {
+    if (va && vb) kernel = sgemm::sgemm_ffma_cp_kernel<T, true, true, ROLE>;
+    else if (va) kernel = sgemm::sgemm_ffma_cp_kernel<T, true, false, ROLE>;
+    else if (vb) kernel = sgemm::sgemm_ffma_cp_kernel<T, false, true, ROLE>;
+    else kernel = sgemm::sgemm_ffma_cp_kernel<T, false, false, ROLE>;
+    return va ? (vb ? cp_packed_attr<T, true, true, ROLE>(dev) : cp_packed_attr<T, true, false, ROLE>(dev))
+              : (vb ? cp_packed_attr<T, false, true, ROLE>(dev) : cp_packed_attr<T, false, false, ROLE>(dev));
+}
+
+// Launch the packed cp.async kernel (operands TMA cannot address) over grouped
+// tiles [tile_base, tile_base + tiles), with the same roles as launch_tma.
+template <class T>
+int launch_cp(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
+              int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
+    const bool va = aligned16(p.A) && p.lda % 4 == 0;
+    const bool vb = aligned16(p.B) && p.ldb % 4 == 0;
+    const int dbg = g_debug_flags.load();
+    void (*kernel)(int, int, int, float, const float *, int, const float *, int, float, float *, int, int, float *,
+                   int, int) = nullptr;
+    if (cs <= 1) {
+        const bool attr = primary ? cp_packed_kernel<T, sgemm::kRolePrimary>(va, vb, info.dev, kernel)
+                                  : cp_packed_kernel<T, sgemm::kRolePlain>(va, vb, info.dev, kernel);
+        if (!attr) return SGEMM_ERR_LAUNCH;
+        const dim3 grid((unsigned)tiles, (unsigned)splits);
+        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p.M, p.N, p.K, alpha, p.A, p.lda, p.B, p.ldb, beta, p.C,
+                                                            p.ldc, vc ? 1 : 0, partials, ldp, (int)tile_base);
+        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
+    if (!cp_packed_kernel<T, sgemm::kRoleSplit>(va, vb, info.dev, kernel)) return SGEMM_ERR_LAUNCH;
+    const bool overlap = tile_base > 0 && !(dbg & kDebugNoOverlap);
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = split_config<T>(tiles, cs, overlap, stream, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p.M, p.N, p.K, alpha, p.A, p.lda, p.B, p.ldb, beta, p.C,
+                                             p.ldc, vc ? 1 : 0, (float *)nullptr, 0, (int)tile_base);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Launch the product kernel over a (tiles x splits) grid.  splits > 1 writes
 // partial sums to `partials` (splits slabs of M x ldp) instead of C.
 int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
@@ -341,19 +377,20 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
         }
         const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
         return launch_tma<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, 0, tiles, 1, false, stream, info);
-    } else {
-        using T = CpTile;
-        const bool vb = aligned16(p.B) && p.ldb % 4 == 0;
-        const bool attr = vb ? (vc ? cp_attr<T, true, true>(info.dev) : cp_attr<T, true, false>(info.dev))
-                             : (vc ? cp_attr<T, false, true>(info.dev) : cp_attr<T, false, false>(info.dev));
-        if (!attr) return SGEMM_ERR_LAUNCH;
-        auto kernel = vb ? (vc ? sgemm::sgemm_ffma_kernel<T, true, true> : sgemm::sgemm_ffma_kernel<T, true, false>)
-                         : (vc ? sgemm::sgemm_ffma_kernel<T, false, true> : sgemm::sgemm_ffma_kernel<T, false, false>);
-        const dim3 grid((unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN)), (unsigned)splits);
-        kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(p.M, p.N, p.K, alpha, p.A, p.lda, p.B, p.ldb, beta, p.C,
-                                                            p.ldc, partials, ldp);
     }
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    // operands the TMA cannot address (and K == 0): the same tile fed by cp.async
+    if (splits == 1) {
+        const SplitPlan plan = split_plan(p.M, p.N, p.K, info);
+        if (plan.full > 0) {
+            const int st =
+                launch_cp<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.full, 1, plan.cs > 1, stream, info);
+            if (st != SGEMM_OK || plan.full == plan.tiles) return st;
+        }
+        return launch_cp<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, plan.full, plan.tiles - plan.full, plan.cs,
+                                  false, stream, info);
+    }
+    const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
+    return launch_cp<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, 0, tiles, 1, false, stream, info);
 }
 
 int launch_reduce(const Problem &p, int splits, const float *partials, int ldp, cudaStream_t stream,
@@ -390,7 +427,7 @@ int validate(const Problem &p) {
         return SGEMM_ERR_INVALID_ARG;
     if (!c_nonempty) return SGEMM_OK;
     // the larger of the two tile grids must fit gridDim.x
-    const int64_t tiles = (int64_t)((p.M + CpTile::BM - 1) / CpTile::BM) * ((p.N + CpTile::BN - 1) / CpTile::BN);
+    const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
     if (tiles > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
     uintptr_t c0, c1, a0, a1, b0, b1;
     span(p.C, p.M, p.N, p.ldc, c0, c1);
@@ -689,7 +726,7 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 3u)
         return SGEMM_ERR_INVALID_ARG;
     if (!c_nonempty) return SGEMM_OK;
-    const int64_t tiles = (int64_t)((M + CpTile::BM - 1) / CpTile::BM) * ((N + CpTile::BN - 1) / CpTile::BN);
+    const int64_t tiles = (int64_t)((M + TmaTile::BM - 1) / TmaTile::BM) * ((N + TmaTile::BN - 1) / TmaTile::BN);
     if (tiles > 0x7fffffff || K > 65535 * 32 || (transb && N > 65535 * 32)) return SGEMM_ERR_INVALID_ARG;
     uintptr_t c0, c1, a0, a1, b0, b1;
     span(C, M, N, ldc, c0, c1);

@@ -63,9 +63,10 @@ typedef enum {
  *     4 floats), K >= 1: 128 x 128 block tiles copied by the tensor memory
  *     accelerator (TMA) with hardware zero-fill at the edges, 8 x 16 outputs
  *     per thread accumulated with packed two-wide FP32 FMAs;
- *   - otherwise: 128 x 128 block tiles copied by cp.async with per-element
- *     masks, 8 x 8 outputs per thread.
- * On the TMA path, when a grid would leave SMs idle (few tiles, or a last
+ *   - otherwise (and for K == 0): the same tiles, fragment reads and packed
+ *     FMAs, fed by cp.async copies with per-element masks (16-byte copies for
+ *     an operand whose rows are 16-byte aligned, 4-byte copies otherwise).
+ * On both paths, when a grid would leave SMs idle (few tiles, or a last
  * partial round of tiles over the SMs), those tiles are each shared by a
  * thread-block cluster of 2, 4 or 8 blocks that split its k-steps and add their
  * partial sums through distributed shared memory in a fixed rank order: no
@@ -83,9 +84,10 @@ int sgemm_f32(int M, int N, int K,
               cudaStream_t stream);
 
 /*
- * How sgemm_f32 launches an M x N x K product with aligned operands (the TMA
- * path, K > 64) on the current device: *tiles = the number of 128 x 128 output
- * tiles; the first *full_tiles of them run as a plain grid, the rest as
+ * How sgemm_f32 launches an M x N x K product on the current device: *tiles =
+ * the number of output tiles (128 x 128; 128 x 64 for aligned operands with
+ * K <= 64, which are never split); the first *full_tiles of them run as a
+ * plain grid, the rest as
  * clusters of *cluster_size blocks that split each tile's k-steps
  * (*cluster_size == 1: no cluster split, *full_tiles == *tiles).  The result
  * reflects the test-only switches of sgemm_debug_set.  Launches nothing.
@@ -318,8 +320,8 @@ int sgemm_device_status(cudaStream_t stream);
  * TEST-ONLY.  flags bit 0: the TMA-fed kernels never issue their copies, so every
  * block's bounded wait runs out (used to check the timeout path without any
  * fault); bit 1: route every product to the cp.async kernel, so both kernels
- * can be checked on the same inputs; bits 4..7: the cluster size of the TMA
- * path's cluster split, forced (0 = automatic, 1 = never split, 2 .. 8 =
+ * can be checked on the same inputs; bits 4..7: the cluster size of the
+ * cluster split, forced (0 = automatic, 1 = never split, 2 .. 8 =
  * split the tiles beyond whole multiples of the SM count with that size);
  * bit 8: with a forced size, split every tile; bit 9: no programmatic overlap
  * of the cluster-split launch with the plain one before it.  wait_limit_ns:
