@@ -50,9 +50,14 @@ L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 FP32_LANES_PER_SM = 128
 MAX_SM_MHZ = 2070.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffma_tma_square_8192.md")
 KERNEL_SOURCES = ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_sgemm.cuh", "dense_fp32_matrix_04_gb300/csrc/ptx.cuh",
                   "dense_fp32_matrix_04_gb300/csrc/tile_map.cuh"]
+# workload -> (committed ncu summary with its DRAM bytes, kernel sources the capture covers)
+TRAFFIC_PROFILES = {
+    "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES),
+    "ragged_3001x4999x2047": ("ffma_cp_ragged_3001x4999x2047.md",
+                              ["dense_fp32_matrix_04_gb300/csrc/ffma_cp_packed.cuh"] + KERNEL_SOURCES),
+}
 
 
 def log(*a):
@@ -204,24 +209,27 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- ncu traffic
 
-def kernel_source_digest():
+def kernel_source_digest(sources=None):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel sources as they are now; else None."""
+def recorded_traffic(workload=DEFAULT_WORKLOAD):
+    """DRAM bytes of one product of the workload from its committed ncu summary,
+    if the capture was taken on the kernel sources as they are now; else None."""
+    if workload not in TRAFFIC_PROFILES:
+        return None
+    name, sources = TRAFFIC_PROFILES[workload]
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
-    if not m or not d or d.group(1) != kernel_source_digest():
+    if not m or not d or d.group(1) != kernel_source_digest(sources):
         return None
     return int(m.group(1))
 
@@ -469,7 +477,7 @@ def run_ours(args):
         roofline = {"bound": "hbm", "achieved": alg_bytes / per_launch_s / 1e9, "peak": hbm_gbs, "unit": "GB/s",
                     "peak_basis": f"copy bandwidth, {hbm_src}"}
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
-    roofline["traffic"] = recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None
+    roofline["traffic"] = recorded_traffic(args.workload) if args.path == "ffma" else None
     roofline["algorithmic_bytes"] = alg_bytes
     roofline["alu_floor_ms"] = t_alu * 1e3
     roofline["hbm_floor_ms"] = t_hbm * 1e3

@@ -45,10 +45,16 @@ def test_workload_config_and_metric_names():
 
 
 def test_recorded_traffic_follows_the_kernel_sources():
-    # the committed ncu summary carries the digest of the kernel headers it was taken on
+    # each committed ncu summary carries the digest of the kernel headers it was taken on
     t = bench.recorded_traffic()
     assert t is None or t > 805_306_368       # at least the algorithmic bytes when present
+    r = bench.recorded_traffic("ragged_3001x4999x2047")
+    assert r is None or r > 4 * (3001 * 2047 + 2047 * 4999 + 3001 * 4999)
+    assert bench.recorded_traffic("tiny_6x6x9") is None
     assert len(bench.kernel_source_digest()) == 16
+    for name, sources in bench.TRAFFIC_PROFILES.values():
+        assert os.path.exists(os.path.join(bench.ROOT, "profiles", name))
+        assert len(bench.kernel_source_digest(sources)) == 16
 
 
 def test_tf32_peak_derivation():
