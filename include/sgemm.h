@@ -20,6 +20,12 @@
  * does not touch host memory behind the caller's back.  Entries of C outside
  * the M x N block (the gap between N and ldc) are never written.
  *
+ * CUDA graphs: the first call on a device does one-time set-up (kernel
+ * shared-memory limits, a cluster occupancy query); after one such call,
+ * sgemm_f32, sgemm_f32_splitk, sgemm_f32_3xtf32 and sgemm_gemm launch only
+ * kernels (and, for sgemm_gemm, device-to-device copies) on `stream`, so they
+ * can be captured into a graph and replayed on new data in the same buffers.
+ *
  * Numerics: each element is an FP32 sum of FP32 products in some order, with
  * round-to-nearest fused multiply-adds; the result satisfies
  * |C - C_exact| <= 2 * K * 2^-24 * sum_k |a_ik| |b_kj| elementwise, and is
