@@ -806,8 +806,8 @@ constexpr int kHostBChunks = 8;
 struct HostPlan {
     int rows;          // rows of C per panel (a multiple of the 128-row tile)
     int panels;
-    int chunks;        // column blocks of B (whole 128-column tiles each)
-    int chunk_cols;    // columns per block (the last one may be narrower)
+    int chunks;                        // column blocks of B (whole 128-column tiles each)
+    int chunk_c0[kHostBChunks + 1];    // first column of each block; chunk_c0[chunks] = N
     int64_t lda_d;     // device row pitch of the A panels (floats)
     int64_t ldn_d;     // device row pitch of B and of the C panels
     size_t b_bytes, a_bytes, c_bytes, total;
@@ -837,15 +837,24 @@ HostPlan host_plan(int M, int N, int K, int panels, int sms) {
     if (rows < 1) rows = 1;
     h.rows = (int)rows;
     h.panels = (int)((M + rows - 1) / rows);
-    // column blocks of B for the first panel: at most kHostBChunks, each wide
-    // enough that the first panel's product over it still gives every SM a tile
+    // column blocks of B for the first panel: the first two just wide enough
+    // that the first panel's product over one still gives every SM a tile, then
+    // doubling widths (each block's copy is shorter than the product over the
+    // block before it, and wide blocks run at two CTAs per SM), the last one
+    // taking the rest
     const int64_t tiles_m0 = (rows + TmaTile::BM - 1) / TmaTile::BM;
-    int64_t per = (tiles_n + kHostBChunks - 1) / kHostBChunks;
     const int64_t fill = ((int64_t)(sms > 0 ? sms : 1) + tiles_m0 - 1) / tiles_m0;
-    if (per < fill) per = fill;
-    if (per > tiles_n) per = tiles_n > 0 ? tiles_n : 1;
-    h.chunk_cols = (int)(per * TmaTile::BN);
-    h.chunks = (int)((N + h.chunk_cols - 1) / h.chunk_cols);
+    int64_t w = fill < 1 ? 1 : fill;
+    int64_t t0 = 0;
+    h.chunks = 0;
+    while (t0 < tiles_n && h.chunks < kHostBChunks) {
+        h.chunk_c0[h.chunks++] = (int)(t0 * TmaTile::BN);
+        int64_t width = h.chunks <= 2 ? w : w << (h.chunks - 2);
+        if (h.chunks == kHostBChunks || t0 + width > tiles_n) width = tiles_n - t0;
+        t0 += width;
+    }
+    if (h.chunks == 0) h.chunk_c0[h.chunks++] = 0;
+    h.chunk_c0[h.chunks] = N;
     h.lda_d = ld4(K);
     h.ldn_d = ld4(N);
     h.b_bytes = (size_t)K * h.ldn_d * sizeof(float);
@@ -937,8 +946,8 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
     };
     if (st == SGEMM_OK) copy_a(0);
     for (int j = 0; j < h.chunks && st == SGEMM_OK; ++j) {
-        const int c0 = j * h.chunk_cols;
-        const int cols = (N - c0) < h.chunk_cols ? (N - c0) : h.chunk_cols;
+        const int c0 = h.chunk_c0[j];
+        const int cols = h.chunk_c0[j + 1] - c0;
         ok(cudaMemcpy2DAsync(dB + c0, h.ldn_d * sizeof(float), B + c0, (size_t)ldb * sizeof(float),
                              (size_t)cols * sizeof(float), K, cudaMemcpyHostToDevice, h2d_stream));
         ok(cudaEventRecord(ev_b[j], h2d_stream));
@@ -956,8 +965,8 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
         // landed; later panels: one product over all of B (every block has landed)
         const int parts = p == 0 ? h.chunks : 1;
         for (int j = 0; j < parts && st == SGEMM_OK; ++j) {
-            const int c0 = p == 0 ? j * h.chunk_cols : 0;
-            const int cols = p == 0 ? ((N - c0) < h.chunk_cols ? (N - c0) : h.chunk_cols) : N;
+            const int c0 = p == 0 ? h.chunk_c0[j] : 0;
+            const int cols = p == 0 ? h.chunk_c0[j + 1] - c0 : N;
             if (p == 0) ok(cudaStreamWaitEvent(stream, ev_b[j], 0));
             if (st != SGEMM_OK) break;
             const Problem prob{rows, cols, K, dA[b], (int)h.lda_d, dB + c0, (int)h.ldn_d, dC[b] + c0, (int)h.ldn_d};

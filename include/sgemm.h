@@ -245,7 +245,8 @@ size_t sgemm_gemm_workspace_size(int algo, int transa, int transb, int M, int N,
 
 /*
  * C = A * B with A, B and C in HOST memory: the end-to-end form of sgemm_f32.
- * B is copied to the device once, in up to 8 column blocks; then, panel by
+ * B is copied to the device once, in up to 8 column blocks of growing width;
+ * then, panel by
  * panel of at most `panels` row panels of C (each rounded up to whole waves of
  * 128 x 128 output tiles on this device, so fewer panels may result), the rows
  * of A are copied in on h2d_stream, the product runs on `stream` with the

@@ -2,9 +2,10 @@
 (which does the per-device set-up: shared-memory limits, the cluster
 occupancy query), sgemm_f32 -- on the plain grid, the cluster split alone,
 the plain grid followed by a programmatically overlapped cluster split, the
-cp.async-fed kernel and the small-K tile -- sgemm_f32_splitk and
-sgemm_f32_3xtf32 are captured with torch.cuda.graph, replayed on new inputs
-written into the same buffers, and must equal the eager results bit for bit."""
+cp.async-fed kernel and the small-K tile -- sgemm_f32_splitk, sgemm_f32_3xtf32
+and sgemm_gemm (both algorithms, A transposed) are captured with
+torch.cuda.graph, replayed on new inputs written into the same buffers, and
+must equal the eager results bit for bit."""
 
 import numpy as np
 import pytest
@@ -74,7 +75,7 @@ def test_sgemm_f32_replays_bitwise(sg, M, N, K, aligned, expect):
     assert sg.sgemm_device_status() == sg.SGEMM_OK
 
 
-def test_splitk_and_3xtf32_replay_bitwise(sg):
+def test_splitk_3xtf32_and_gemm_replay_bitwise(sg):
     import torch
     M, N, K = 768, 640, 3000
     A, B, C = _buffers(torch, M, N, K, True)
@@ -83,9 +84,19 @@ def test_splitk_and_3xtf32_replay_bitwise(sg):
     w3 = torch.empty(sg.sgemm_f32_3xtf32_workspace_size(M, N, K) // 4 + 4, device="cuda")
     C3 = torch.empty_like(C)
 
+    # sgemm_gemm on both algorithms with A stored transposed (K x M) into its own workspace
+    At = torch.zeros(K, M, device="cuda")
+    Cg = [torch.zeros(M, N, device="cuda") for _ in range(2)]
+    wg = [torch.empty(max(sg.sgemm_gemm_workspace_size(algo, 1, 0, M, N, K) // 4, 4) + 4, device="cuda")
+          for algo in (0, 1)]
+
     def step():
         sg.matmul_splitk(A, B, out=C, splits=splits, workspace=wk)
         sg.matmul_3xtf32(A, B, out=C3, workspace=w3)
+        At.copy_(A.t())
+        for algo in (0, 1):
+            sg.sgemm_gemm(algo, 1, 0, M, N, K, 0.5, At, M, B, B.stride(0), 0.25, Cg[algo], N, wg[algo],
+                          wg[algo].numel() * 4)
     a0, b0 = gen.operands(M, N, K, seed=403)
     A.copy_(torch.from_numpy(a0))
     B.copy_(torch.from_numpy(b0))
@@ -101,10 +112,17 @@ def test_splitk_and_3xtf32_replay_bitwise(sg):
     a, b = gen.operands(M, N, K, seed=404)
     A.copy_(torch.from_numpy(a))
     B.copy_(torch.from_numpy(b))
+    prev = Cg[0].clone()                 # C = 0.5 op(A) B + 0.25 C reads C: replay and eager start alike
+    Cg[1].copy_(prev)
     g.replay()
     torch.cuda.synchronize()
     got, got3 = C.clone(), C3.clone()
+    got_g = [c.clone() for c in Cg]
+    for c in Cg:
+        c.copy_(prev)
     step()
     torch.cuda.synchronize()
     assert torch.equal(got, C) and torch.equal(got3, C3)
+    for algo in (0, 1):
+        assert torch.equal(got_g[algo], Cg[algo])
     assert sg.sgemm_device_status() == sg.SGEMM_OK
