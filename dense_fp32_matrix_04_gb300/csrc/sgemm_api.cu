@@ -36,11 +36,12 @@ using X3Tile = sgemm::Tf32x3MainTile;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 64;
 
-// test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernel.
-// Bits 4..7: cluster size forced on the TMA path's cluster split (0 = the
-// automatic plan, 1 = never split, 2 .. 8 = split the tiles beyond whole
-// multiples of the SM count with that cluster size); bit 8: put every tile in
-// the cluster-split launch; bit 9 below.
+// test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernels.
+// Bit 1: route every product to the cp.async-fed kernel.  Bits 4..7: cluster
+// size forced on the cluster split (0 = the automatic plan, 1 = never split,
+// 2 .. 8 = split the tiles beyond whole multiples of the SM count with that
+// cluster size); bit 8: put every tile in the cluster-split launch; bit 9: no
+// programmatic overlap.
 constexpr int kDebugForceCpAsync = 2;
 constexpr int kDebugClusterShift = 4;
 constexpr int kDebugClusterAll = 256;
@@ -167,7 +168,8 @@ cudaLaunchConfig_t split_config(int64_t clusters, int cs, bool overlap, cudaStre
 }
 
 // Whether clusters of `cs` CTAs of the cluster-split kernel can be resident on
-// this device at all; queried once per device and size.
+// this device at all; queried once per device and size on the TMA form (the
+// cp.async form has the same block size, shared memory and CTAs per SM).
 template <class T>
 bool cluster_fits(int dev, int cs) {
     static std::atomic<int> known[kMaxDevices][9];  // 0 unknown, 1 yes, 2 no
@@ -190,9 +192,9 @@ bool cluster_fits(int dev, int cs) {
     return k == 1;
 }
 
-// How a product on the TMA main tile is launched: tiles [0, full) as a plain
-// grid, tiles [full, tiles) as clusters of `cs` CTAs that split each tile's
-// k-steps (cs == 1: no cluster split).
+// How a product on the main tile (TMA or cp.async-fed) is launched: tiles
+// [0, full) as a plain grid, tiles [full, tiles) as clusters of `cs` CTAs that
+// split each tile's k-steps (cs == 1: no cluster split).
 struct SplitPlan {
     int64_t tiles = 0;
     int64_t full = 0;
@@ -352,45 +354,36 @@ int launch_cp(const Problem &p, float alpha, float beta, bool vc, int splits, fl
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
-// Launch the product kernel over a (tiles x splits) grid.  splits > 1 writes
-// partial sums to `partials` (splits slabs of M x ldp) instead of C.
+// Launch the product: on the TMA kernels when the operands allow it (the
+// small-K tile for K <= 64), otherwise on the cp.async-fed kernel.  splits > 1
+// writes partial sums to `partials` (splits slabs of M x ldp) instead of C;
+// splits == 1 follows the cluster-split plan.
 int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
                    const DeviceInfo &info) {
     const bool vc = splits > 1 || (aligned16(p.C) && p.ldc % 4 == 0);
     // partial slabs hold the raw products; alpha and beta act in the reduction
     const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
-    if (use_tma(p)) {
-        if (splits == 1 && p.K <= 2 * TmaSmallK::BK) {
-            const int64_t tiles =
-                (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
-            return launch_tma<TmaSmallK>(p, alpha, beta, vc, 1, partials, ldp, 0, tiles, 1, false, stream, info);
-        }
-        if (splits == 1) {
-            const SplitPlan plan = split_plan(p.M, p.N, p.K, info);
-            if (plan.full > 0) {
-                const int st =
-                    launch_tma<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.full, 1, plan.cs > 1, stream, info);
-                if (st != SGEMM_OK || plan.full == plan.tiles) return st;
-            }
-            return launch_tma<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, plan.full, plan.tiles - plan.full,
-                                       plan.cs, false, stream, info);
-        }
+    const bool tma = use_tma(p);
+    if (tma && splits == 1 && p.K <= 2 * TmaSmallK::BK) {
+        const int64_t tiles =
+            (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
+        return launch_tma<TmaSmallK>(p, alpha, beta, vc, 1, partials, ldp, 0, tiles, 1, false, stream, info);
+    }
+    // grouped tiles [base, base + n) as a (n x s) grid, or n clusters of cs CTAs
+    auto launch = [&](int64_t base, int64_t n, int s, int cs, bool primary) {
+        return tma ? launch_tma<TmaTile>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream, info)
+                   : launch_cp<TmaTile>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream, info);
+    };
+    if (splits > 1) {
         const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
-        return launch_tma<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, 0, tiles, 1, false, stream, info);
+        return launch(0, tiles, splits, 1, false);
     }
-    // operands the TMA cannot address (and K == 0): the same tile fed by cp.async
-    if (splits == 1) {
-        const SplitPlan plan = split_plan(p.M, p.N, p.K, info);
-        if (plan.full > 0) {
-            const int st =
-                launch_cp<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.full, 1, plan.cs > 1, stream, info);
-            if (st != SGEMM_OK || plan.full == plan.tiles) return st;
-        }
-        return launch_cp<TmaTile>(p, alpha, beta, vc, 1, partials, ldp, plan.full, plan.tiles - plan.full, plan.cs,
-                                  false, stream, info);
+    const SplitPlan plan = split_plan(p.M, p.N, p.K, info);
+    if (plan.full > 0) {
+        const int st = launch(0, plan.full, 1, 1, plan.cs > 1);
+        if (st != SGEMM_OK || plan.full == plan.tiles) return st;
     }
-    const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
-    return launch_cp<TmaTile>(p, alpha, beta, vc, splits, partials, ldp, 0, tiles, 1, false, stream, info);
+    return launch(plan.full, plan.tiles - plan.full, 1, plan.cs, false);
 }
 
 int launch_reduce(const Problem &p, int splits, const float *partials, int ldp, cudaStream_t stream,
@@ -426,8 +419,9 @@ int validate(const Problem &p) {
     if ((reinterpret_cast<uintptr_t>(p.A) | reinterpret_cast<uintptr_t>(p.B) | reinterpret_cast<uintptr_t>(p.C)) & 3u)
         return SGEMM_ERR_INVALID_ARG;
     if (!c_nonempty) return SGEMM_OK;
-    // the larger of the two tile grids must fit gridDim.x
-    const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
+    // the largest tile grid (the small-K tile's 128 x 64 tiles) must fit gridDim.x
+    const int64_t tiles =
+        (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
     if (tiles > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
     uintptr_t c0, c1, a0, a1, b0, b1;
     span(p.C, p.M, p.N, p.ldc, c0, c1);
@@ -726,7 +720,7 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 3u)
         return SGEMM_ERR_INVALID_ARG;
     if (!c_nonempty) return SGEMM_OK;
-    const int64_t tiles = (int64_t)((M + TmaTile::BM - 1) / TmaTile::BM) * ((N + TmaTile::BN - 1) / TmaTile::BN);
+    const int64_t tiles = (int64_t)((M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((N + TmaSmallK::BN - 1) / TmaSmallK::BN);
     if (tiles > 0x7fffffff || K > 65535 * 32 || (transb && N > 65535 * 32)) return SGEMM_ERR_INVALID_ARG;
     uintptr_t c0, c1, a0, a1, b0, b1;
     span(C, M, N, ldc, c0, c1);
