@@ -275,11 +275,19 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
 
         def step():
             sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, ws_bytes, handle)
-        return step, 3
+        return step, x3_launches(sg, M, N, K)
 
     def step():
         sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N, handle)
     return step, f32_launches(sg, M, N, K)
+
+
+def x3_launches(sg, M, N, K):
+    """Kernels one sgemm_f32_3xtf32 call launches: the two split passes and the
+    tensor-core product, plus the reduction when the product is divided (its
+    workspace then holds partial tiles beyond the split operands)."""
+    operands = (4 * ((K + 3) // 4 * 4) * (2 * M + 2 * N) + 255) // 256 * 256
+    return 4 if sg.sgemm_f32_3xtf32_workspace_size(M, N, K) > operands else 3
 
 
 def f32_launches(sg, M, N, K):

@@ -451,9 +451,37 @@ size_t partials_bytes(int M, int N, int splits) {
 // Row length of the split operands in the 3xTF32 workspace (16-byte rows for TMA).
 int64_t x3_kpad(int K) { return ((int64_t)K + 3) / 4 * 4; }
 
-size_t x3_workspace_bytes(int M, int N, int K) {
+// Split count of the 3xTF32 product: its kernel runs one CTA per SM, so a grid
+// of fewer than half as many 128 x 256 tiles as SMs has its k-steps divided
+// among CTA rows (up to 16, keeping at least eight 16-deep k-steps each), and
+// the partial tiles are added in row order by the split-K reduction.
+int x3_splits(int M, int N, int K, int sms) {
+    using T = X3Tile;
+    if (M <= 0 || N <= 0 || K <= 0 || sms <= 0) return 1;
+    const int64_t tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
+    const int64_t kt = (K + T::BK - 1) / T::BK;
+    if (2 * tiles > sms) return 1;
+    int64_t s = sms / tiles;
+    if (s > kt / 8) s = kt / 8;
+    if (s > 16) s = 16;
+    if (s < 2) return 1;
+    const int64_t per = (kt + s - 1) / s;  // no empty splits
+    return (int)((kt + per - 1) / per);
+}
+
+int64_t up256(int64_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace of a 3xTF32 product: the split operands (A_hi, A_lo: M x K_pad;
+// B_hi^T, B_lo^T: N x K_pad), then the partial tiles of a split-K product.
+size_t x3_workspace_bytes(int M, int N, int K, int sms) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    return (size_t)(4 * x3_kpad(K) * (2 * (int64_t)M + 2 * (int64_t)N));
+    const int64_t ops = 4 * x3_kpad(K) * (2 * (int64_t)M + 2 * (int64_t)N);
+    return (size_t)(up256(ops) + (int64_t)partials_bytes(M, N, x3_splits(M, N, K, sms)));
+}
+
+int device_sms() {
+    DeviceInfo info;
+    return device_info(info) == SGEMM_OK ? info.sms : 0;
 }
 
 // The four launches of a 3xTF32 product: split A, split and transpose B, then
@@ -490,13 +518,24 @@ int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const Device
         return SGEMM_ERR_LAUNCH;
     const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
     static std::atomic<int> done_v[kMaxDevices], done_s[kMaxDevices];
-    if (!(vc ? smem_attr_once(done_v[info.dev], sgemm::sgemm_3xtf32_kernel<T, true>, T::SMEM_BYTES)
-             : smem_attr_once(done_s[info.dev], sgemm::sgemm_3xtf32_kernel<T, false>, T::SMEM_BYTES)))
+    if (!smem_attr_once(done_v[info.dev], sgemm::sgemm_3xtf32_kernel<T, true>, T::SMEM_BYTES) ||
+        (!vc && !smem_attr_once(done_s[info.dev], sgemm::sgemm_3xtf32_kernel<T, false>, T::SMEM_BYTES)))
         return SGEMM_ERR_LAUNCH;
     auto kernel = vc ? sgemm::sgemm_3xtf32_kernel<T, true> : sgemm::sgemm_3xtf32_kernel<T, false>;
     const unsigned tiles = (unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN));
+    const int splits = x3_splits(p.M, p.N, p.K, info.sms);
+    float *partials = ws + up256(4 * kp * (2 * (int64_t)p.M + 2 * (int64_t)p.N)) / 4;
+    const int ldp = ld_partials(p.N);
+    if (splits > 1) {
+        // the kernel writes raw partial tiles; alpha and beta act in the reduction
+        sgemm::sgemm_3xtf32_kernel<T, true><<<dim3(tiles, (unsigned)splits), T::THREADS, T::SMEM_BYTES, stream>>>(
+            tah, tal, tbh, tbl, p.M, p.N, p.K, 1.f, 0.f, partials, ldp, partials, ldp, info.err_word,
+            g_wait_limit_ns.load(), g_debug_flags.load());
+        if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        return launch_reduce(p, splits, partials, ldp, stream, info);
+    }
     kernel<<<tiles, T::THREADS, T::SMEM_BYTES, stream>>>(tah, tal, tbh, tbl, p.M, p.N, p.K, p.alpha, p.beta, p.C, p.ldc,
-                                                         info.err_word, g_wait_limit_ns.load(),
+                                                         nullptr, 0, info.err_word, g_wait_limit_ns.load(),
                                                          g_debug_flags.load());
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
@@ -641,7 +680,7 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const
     return launch_reduce(p, splits, scratch, ldp, stream, info);
 }
 
-size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K) { return x3_workspace_bytes(M, N, K); }
+size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K) { return x3_workspace_bytes(M, N, K, device_sms()); }
 
 int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
                      float *workspace, size_t workspace_bytes, cudaStream_t stream) {
@@ -650,7 +689,7 @@ int sgemm_f32_3xtf32(int M, int N, int K, const float *A, int lda, const float *
     if (st != SGEMM_OK || (int64_t)M * N == 0) return st;
     if (K > 65535 * 32) return SGEMM_ERR_INVALID_ARG;
     if (K == 0) return sgemm_f32(M, N, K, A, lda, B, ldb, C, ldc, stream);  // an empty sum: zeros
-    const size_t need = x3_workspace_bytes(M, N, K);
+    const size_t need = x3_workspace_bytes(M, N, K, device_sms());
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
     const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + need;
     uintptr_t lo, hi;
@@ -699,7 +738,7 @@ int sgemm_f32_ladder(int level, int M, int N, int K, const float *A, int lda, co
 }
 
 size_t sgemm_gemm_workspace_size(int algo, int transa, int transb, int M, int N, int K) {
-    if (algo == SGEMM_ALGO_3XTF32) return x3_workspace_bytes(M, N, K);
+    if (algo == SGEMM_ALGO_3XTF32) return x3_workspace_bytes(M, N, K, device_sms());
     return gemm_ffma_workspace(transa, transb, M, N, K);
 }
 

@@ -141,12 +141,16 @@ __device__ __forceinline__ uint64_t umma_desc_swizzled(uint32_t saddr, uint32_t 
            ((uint64_t)1u << 46) | ((uint64_t)layout << 61);
 }
 
+// Split-K: CTA row blockIdx.y takes an equal run of the k-steps; with more
+// than one row, each writes its partial tile to its own M x ldp slab of
+// `partials` (the host then adds the slabs in row order into C).
 template <class T, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, 1)
     sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
                         const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, int M,
                         int N, int K, float alpha, float beta, float *__restrict__ C, int ldc,
-                        int *__restrict__ err_word, unsigned long long wait_limit_ns, int debug) {
+                        float *__restrict__ partials, int ldp, int *__restrict__ err_word,
+                        unsigned long long wait_limit_ns, int debug) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -161,7 +165,14 @@ __global__ void __launch_bounds__(T::THREADS, 1)
     int tile_m, tile_n;
     grouped_tile<8>(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
     const int m0 = tile_m * T::BM, n0 = tile_n * T::BN;
-    const int KT = (K + T::BK - 1) / T::BK;
+    const int KT_all = (K + T::BK - 1) / T::BK;
+    const int per_split = (KT_all + gridDim.y - 1) / gridDim.y;
+    const int kt_begin = blockIdx.y * per_split;
+    const int KT = max(0, min(KT_all, kt_begin + per_split) - kt_begin);  // 0: this split's partial is zero
+    if (gridDim.y > 1) {
+        C = partials + (int64_t)blockIdx.y * M * ldp;
+        ldc = ldp;
+    }
 
     if (warp == 0) {
         tmem_alloc(smem_addr(tmem_slot), T::TMEM_COLS);
@@ -198,10 +209,11 @@ __global__ void __launch_bounds__(T::THREADS, 1)
             if (*abort_flag) break;
             const uint32_t dst = base + s * T::STAGE, bar = full0 + 8 * s;
             mbar_arrive_expect_tx(bar, T::STAGE);
-            tma_load_2d(dst, &tmAh, kt * T::BK, m0, bar);
-            tma_load_2d(dst + T::A_BYTES, &tmAl, kt * T::BK, m0, bar);
-            tma_load_2d(dst + 2 * T::A_BYTES, &tmBh, kt * T::BK, n0, bar);
-            tma_load_2d(dst + 2 * T::A_BYTES + T::B_BYTES, &tmBl, kt * T::BK, n0, bar);
+            const int kx = (kt_begin + kt) * T::BK;
+            tma_load_2d(dst, &tmAh, kx, m0, bar);
+            tma_load_2d(dst + T::A_BYTES, &tmAl, kx, m0, bar);
+            tma_load_2d(dst + 2 * T::A_BYTES, &tmBh, kx, n0, bar);
+            tma_load_2d(dst + 2 * T::A_BYTES + T::B_BYTES, &tmBl, kx, n0, bar);
             issued = kt + 1;
         }
         if (*abort_flag) {
@@ -248,6 +260,11 @@ __global__ void __launch_bounds__(T::THREADS, 1)
         for (int c0 = 0; c0 < T::BN; c0 += 32) {
             float v[32];
             tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)c0, v);
+            if (KT == 0) {
+                // no MMA wrote the accumulator: this split's partial sums are zero
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
             if (row < M) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {

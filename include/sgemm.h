@@ -119,7 +119,10 @@ int sgemm_f32_plan(int M, int N, int K, long long *tiles, long long *full_tiles,
  *           aligned, not overlapping A, B or C; its contents on entry do not
  *           matter and on return are unspecified.
  * SGEMM_ERR_INVALID_ARG for a bad split count or a missing, misaligned or
- * short workspace; SGEMM_ERR_ALIAS if the workspace overlaps an operand.
+ * short workspace; SGEMM_ERR_ALIAS if the workspace overlaps an operand.  If
+ * a product kernel gives up on a bounded wait (SGEMM_ERR_TIMEOUT from
+ * sgemm_device_status), the reduction still runs and C holds unspecified
+ * values.
  */
 int sgemm_f32_splitk(int M, int N, int K,
                      const float *A, int lda,
@@ -155,13 +158,20 @@ int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
  * integers are split exactly (A_lo = 0), so integer products whose partial
  * sums stay below 2^24 are exact.
  *
+ * A grid of fewer than half as many 128 x 256 output tiles as the device has
+ * SMs (e.g. 1024 x 1024 x 1024) has its k-steps divided among up to 16 rows
+ * of thread blocks; their partial tiles land in the workspace and are added
+ * in row order into C (deterministic, the same bound).
+ *
  * workspace: caller-owned device memory of at least
  * sgemm_f32_3xtf32_workspace_size(M, N, K) bytes, 16-byte aligned, not
  * overlapping A, B or C; it receives A_hi, A_lo (M x K) and B_hi, B_lo
- * transposed (N x K), with rows padded to a multiple of 4 floats.  Any
- * alignment of A, B and C is accepted.  K <= 2,097,120.  K == 0 writes zeros
- * and needs no workspace.  Errors as for sgemm_f32_splitk; the copy waits are
- * bounded and report through sgemm_device_status.
+ * transposed (N x K), with rows padded to a multiple of 4 floats, then the
+ * partial tiles of a divided product.  Any alignment of A, B and C is
+ * accepted.  K <= 2,097,120.  K == 0 writes zeros and needs no workspace.
+ * Errors as for sgemm_f32_splitk; the copy waits are bounded and report
+ * through sgemm_device_status (after a timeout of a divided product C holds
+ * unspecified values).
  */
 int sgemm_f32_3xtf32(int M, int N, int K,
                      const float *A, int lda,
@@ -170,7 +180,9 @@ int sgemm_f32_3xtf32(int M, int N, int K,
                      float *workspace, size_t workspace_bytes,
                      cudaStream_t stream);
 
-/* Workspace bytes sgemm_f32_3xtf32 needs: 4 * (2M + 2N) * (K rounded up to 4). */
+/* Workspace bytes sgemm_f32_3xtf32 needs on the current device: 4 (2M + 2N)
+ * (K rounded up to 4), rounded up to 256, plus splits * M * (N rounded up to
+ * 4) * 4 when the product is divided. */
 size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K);
 
 /*

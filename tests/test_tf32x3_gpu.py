@@ -141,3 +141,81 @@ def test_timeout_path(sg):
     sg.sgemm_f32_3xtf32(128, 256, 64, dA, 64, dB, 256, dC, 256, ws, need)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)
+
+
+# ---------------------------------------------------------------- split-K for small grids
+
+def _operand_bytes(M, N, K):
+    kpad = (K + 3) // 4 * 4
+    return (4 * kpad * (2 * M + 2 * N) + 255) // 256 * 256
+
+
+def _expected_splits(M, N, K, sms):
+    """The split rule restated: fewer than sms / 2 tiles of 128 x 256 -> up to
+    16 rows of blocks, at least eight 16-deep k-steps each, no empty row."""
+    tiles = -(-M // 128) * -(-N // 256)
+    kt = -(-K // 16)
+    if 2 * tiles > sms:
+        return 1
+    s = min(sms // tiles, kt // 8, 16)
+    if s < 2:
+        return 1
+    per = -(-kt // s)
+    return -(-kt // per)
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(256, 256, 4096, 80), (1024, 1024, 1024, 81), (300, 200, 1000, 82),
+                                        (129, 500, 777, 83)])
+def test_divided_products(sg, M, N, K, seed):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits = _expected_splits(M, N, K, sms)
+    assert splits > 1
+    ldp = (N + 3) // 4 * 4
+    assert sg.sgemm_f32_3xtf32_workspace_size(M, N, K) == _operand_bytes(M, N, K) + splits * M * ldp * 4
+    A, B = gen.operands(M, N, K, seed=seed)
+    check_full(run_x3(sg, A, B), A, B)
+
+
+def test_divided_product_integers_and_repeatability(sg):
+    import torch
+    A = gen.matrix(84, gen.STREAM_A_INT, 512, 2048, "int")
+    B = gen.matrix(84, gen.STREAM_B_INT, 2048, 300, "int")
+    C = run_x3(sg, A, B)
+    check_full(C, A, B, exact=True)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    c1 = sg.matmul_3xtf32(dA, dB)
+    c2 = sg.matmul_3xtf32(dA, dB)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+def test_divided_product_alpha_beta(sg):
+    from oracle import ref_gemm, tolerance
+    from test_gemm_general_gpu import run_gemm
+    A = gen.matrix(85, gen.STREAM_A, 3000, 400)      # stored K x M: op(A) = A^T is 400 x 3000
+    B = gen.matrix(85, gen.STREAM_B, 3000, 300)
+    C0 = gen.matrix(86, gen.STREAM_A, 400, 300)
+    C = run_gemm(sg, 1, 1, 0, -1.5, A, B, 0.75, C0)
+    C64, S, T = ref_gemm.gemm_general_f64(True, False, -1.5, A, B, 0.75, C0)
+    assert tolerance.max_error_ratio_general(C, C64, S, T, 3000, -1.5) <= 1.0
+
+
+def test_divided_product_timeout_reports(sg):
+    import torch
+    M, N, K = 256, 256, 2048
+    A, B = gen.operands(M, N, K, seed=87)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.empty(M, N, device="cuda")
+    need = sg.sgemm_f32_3xtf32_workspace_size(M, N, K)
+    assert need > _operand_bytes(M, N, K)
+    ws = torch.empty(need // 4, device="cuda")
+    try:
+        sg.sgemm_debug_set(1, 50_000_000)
+        sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, need)
+        assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
+    finally:
+        sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, need)
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    check_full(dC.cpu().numpy(), A, B)
