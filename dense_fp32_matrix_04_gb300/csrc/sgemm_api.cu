@@ -899,6 +899,33 @@ HostPlan host_plan(int M, int N, int K, int panels, int sms) {
     return h;
 }
 
+// The host pipeline's events, created on a thread's first call for a device
+// and reused by its later calls there: a stream wait takes the event's latest
+// record at the moment it is enqueued, so recording the same event again in a
+// later call is safe.  They live until the process exits.
+constexpr int kHostEvents = 1 + kHostBChunks + 8;
+
+int host_events(int dev, cudaEvent_t *&out) {
+    struct Pool {
+        cudaEvent_t ev[kHostEvents];
+        bool ready = false;
+    };
+    thread_local Pool pool[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    Pool &p = pool[dev];
+    if (!p.ready) {
+        for (int i = 0; i < kHostEvents; ++i) {
+            if (cudaEventCreateWithFlags(&p.ev[i], cudaEventDisableTiming) != cudaSuccess) {
+                for (int j = 0; j < i; ++j) cudaEventDestroy(p.ev[j]);
+                return SGEMM_ERR_LAUNCH;
+            }
+        }
+        p.ready = true;
+    }
+    out = p.ev;
+    return SGEMM_OK;
+}
+
 }  // namespace
 
 size_t sgemm_f32_host_workspace_size(int M, int N, int K, int panels) {
@@ -937,22 +964,17 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
 
     // events: call start; each column block of B landed; A panel landed; A
     // panel consumed; C panel ready; C panel copied out
-    cudaEvent_t ev_start, ev_b[kHostBChunks], ev_a[2], ev_a_free[2], ev_c[2], ev_c_free[2];
-    cudaEvent_t *all[1 + kHostBChunks + 8];
-    int n_ev = 0;
-    all[n_ev++] = &ev_start;
-    for (int j = 0; j < h.chunks; ++j) all[n_ev++] = &ev_b[j];
-    for (cudaEvent_t *e : {&ev_a[0], &ev_a[1], &ev_a_free[0], &ev_a_free[1], &ev_c[0], &ev_c[1], &ev_c_free[0],
-                           &ev_c_free[1]})
-        all[n_ev++] = e;
-    int made = 0;
-    int st = SGEMM_OK;
-    for (int i = 0; i < n_ev; ++i) {
-        if (cudaEventCreateWithFlags(all[i], cudaEventDisableTiming) != cudaSuccess) {
-            st = SGEMM_ERR_LAUNCH;
-            break;
-        }
-        ++made;
+    cudaEvent_t *ev = nullptr;
+    int st = host_events(info.dev, ev);
+    cudaEvent_t ev_start = nullptr, *ev_b = nullptr, *ev_a = nullptr, *ev_a_free = nullptr, *ev_c = nullptr,
+                *ev_c_free = nullptr;
+    if (st == SGEMM_OK) {
+        ev_start = ev[0];
+        ev_b = ev + 1;
+        ev_a = ev + 1 + kHostBChunks;
+        ev_a_free = ev_a + 2;
+        ev_c = ev_a + 4;
+        ev_c_free = ev_a + 6;
     }
     auto ok = [&](cudaError_t e) {
         if (e != cudaSuccess && st == SGEMM_OK) st = SGEMM_ERR_LAUNCH;
@@ -1021,7 +1043,6 @@ int sgemm_f32_host(int M, int N, int K, const float *A, int lda, const float *B,
         ok(cudaStreamWaitEvent(stream, ev_c_free[last], 0));
         if (h.panels >= 2) ok(cudaStreamWaitEvent(stream, ev_c_free[last ^ 1], 0));
     }
-    for (int i = 0; i < made; ++i) cudaEventDestroy(*all[i]);
     return st;
 }
 
