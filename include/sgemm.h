@@ -93,10 +93,10 @@ int sgemm_f32(int M, int N, int K,
  * How sgemm_f32 launches an M x N x K product on the current device: *tiles =
  * the number of output tiles (128 x 128; 128 x 64 for aligned operands with
  * K <= 64, which are never split); the first *full_tiles of them run as a
- * plain grid, the rest as
- * clusters of *cluster_size blocks that split each tile's k-steps
- * (*cluster_size == 1: no cluster split, *full_tiles == *tiles).  The result
- * reflects the test-only switches of sgemm_debug_set.  Launches nothing.
+ * plain grid, the rest as clusters of *cluster_size blocks that split each
+ * tile's k-steps (*cluster_size == 1: no cluster split, *full_tiles ==
+ * *tiles).  The result reflects the test-only switches of sgemm_debug_set.
+ * Launches nothing.
  * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
  * if the device cannot be queried.
  */
