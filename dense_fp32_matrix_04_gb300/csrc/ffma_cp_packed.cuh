@@ -13,10 +13,16 @@
 //    operand's rows are 16-byte aligned it uses 16-byte copies instead.
 //  * Masking: slots outside A or B are zero-filled by the copy itself (source
 //    size 0, no global read) -- the pages' masked tile loads ("SGEMM: Shared
-//    Memory Tiling Visualizer", the tiled kernel listing).
+//    Memory Tiling Visualizer", the tiled kernel listing).  Most copies need
+//    no mask at all: a last, partial row tile reads the 128 rows that end at
+//    row M (and stores only its own), and B's right edge is a per-thread copy
+//    size, so only the last, partial k-step and products with M < 128 take
+//    the masked path.
 //  * Pipeline: STAGES slabs in flight as cp.async groups, one CTA barrier per
 //    k-step; the copy of step t + STAGES - 1 overlaps the FMAs of step t
-//    ("Shared Memory Tiling", 'What tiling does not fix').
+//    ("Shared Memory Tiling", 'What tiling does not fix').  With 4-byte
+//    copies of A, the unmasked copies go out an eighth at a time between the
+//    groups of FMAs instead of in one burst.
 //  * No bounded waits are needed: cp.async groups complete on their own.
 #pragma once
 
@@ -37,6 +43,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                          const float *__restrict__ B, int ldb, float beta, float *__restrict__ C, int ldc,
                          int vec_c, float *__restrict__ partials, int ldp, int tile_base) {
     constexpr bool CSPLIT = ROLE == kRoleSplit;
+    // 4-byte copies of A are spread through the FMAs of the step before (32 per
+    // thread and step otherwise come in one burst).  16-byte copies of A, and
+    // the cluster split's short k-ranges (a quarter of whose steps issue no
+    // copy, so both loop bodies would be live in the SM's instruction cache),
+    // measured faster in one burst.
+    constexpr bool SPREAD = !VEC_A && ROLE != kRoleSplit;
     static_assert(T::PACKED && T::THREADS == 128 && T::BM == 128 && T::BN == 128 && T::BK == 32,
                   "the copy roles below are laid out for 128 threads and 128 x 128 x 32 tiles");
     static_assert(T::STAGES >= 2, "the cp.async pipeline needs two stages");
@@ -60,6 +72,11 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     grouped_tile<8>(tile_base + (CSPLIT ? (int)cluster_id_x() : (int)blockIdx.x), tiles_m, tiles_n, tile_m, tile_n);
     const int m0 = tile_m * T::BM;
     const int n0 = tile_n * T::BN;
+    // The copies read rows m0c .. m0c + BM - 1 of A: a last, partial row tile is
+    // moved up to end at row M (when M >= BM), so that none of its copies needs
+    // a row mask; the rows it then covers twice are left to the tile above.
+    const bool shift_m = M >= T::BM;
+    const int m0c = shift_m ? min(m0, M - T::BM) : m0;
     // split-K by CTA row (partial slabs) or by cluster rank, as in the TMA kernel
     const int KT_all = (K + T::BK - 1) / T::BK;
     const int parts = CSPLIT ? cs : (int)gridDim.y;
@@ -83,34 +100,32 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     const int a_row0 = VEC_A ? 4 * warp + (lane >> 3) : warp;
     constexpr int A_ROW_STEP = VEC_A ? 16 : 4;
     const int a_k = VEC_A ? (lane & 7) * 4 : lane;
-    uint32_t a_rows_ok = 0;  // bit j: row of copy j lies inside A
-#pragma unroll
-    for (int j = 0; j < A_COPIES; ++j)
-        if (m0 + a_row0 + j * A_ROW_STEP < M) a_rows_ok |= 1u << j;
-    const float *gA = A + (int64_t)(m0 + a_row0) * lda + a_k;
-    const int64_t a_step = (int64_t)A_ROW_STEP * lda;
+    const float *gA = A + (int64_t)(m0c + a_row0) * lda + a_k;
+    const int a_step = A_ROW_STEP * lda;  // fits an int: the host checks A_ROW_STEP * lda
     // shared offsets of copy 0 and (4-byte copies) copy 1; copy j adds
     // (j / 2) * 1024 (4-byte) or j * 2048 (16-byte) to the one of its parity
     auto a_off = [&](int r) { return (uint32_t)(r * 128 + ((((a_k >> 2) ^ (r & 7))) << 4) + (VEC_A ? 0 : (a_k & 3) * 4)); };
     const uint32_t a_off0 = a_off(a_row0), a_off1 = a_off(a_row0 + A_ROW_STEP);
     // B, 4-byte: warp w copies columns 32 w + lane of k-rows j (j < 32).
     // B, 16-byte: k-rows 4 j + w (j < 8), columns 4 lane .. 4 lane + 3.
+    // A thread's columns are the same in every k-step, so the right edge is a
+    // per-thread copy size (zero past column N, from a column inside B).
     constexpr int B_COPIES = VEC_B ? 8 : 32;
     const int b_col = VEC_B ? 4 * lane : 32 * warp + lane;
     const int b_krow0 = VEC_B ? warp : 0;
     constexpr int B_KROW_STEP = VEC_B ? 4 : 1;
     const int b_left = N - (n0 + b_col);
     const int b_bytes = VEC_B ? (b_left >= 4 ? 16 : (b_left > 0 ? 4 * b_left : 0)) : (b_left > 0 ? 4 : 0);
-    const float *gB = B + (int64_t)b_krow0 * ldb + n0 + b_col;
-    const int64_t b_step = (int64_t)B_KROW_STEP * ldb;
+    const float *gB = B + (int64_t)b_krow0 * ldb + (b_left > 0 ? n0 + b_col : 0);
+    const int b_step = B_KROW_STEP * ldb;  // likewise
     const uint32_t b_off0 = (uint32_t)(T::A_STAGE + b_krow0 * (T::BN * 4) + b_col * 4);
-    const bool full_mn = m0 + T::BM <= M && n0 + T::BN <= N;
 
-    // Issue the copies of k-step kt (counted from kt_begin) into stage s.  FULL:
-    // the whole 128 x 32 and 32 x 128 slabs lie inside A and B, so no copy needs
-    // a mask.
-    auto issue_impl = [&](auto full_tag, int kt, int s) {
+    // Issue copies of k-step kt (counted from kt_begin) into stage s: group grp
+    // of NG equal groups.  FULL: the step's 32 k lie inside K and the rows of A
+    // inside M, so only B's per-thread size masks anything.
+    auto issue_impl = [&](auto full_tag, auto ng_tag, int kt, int s, int grp) {
         constexpr bool FULL = decltype(full_tag)::value;
+        constexpr int NG = decltype(ng_tag)::value;
         const int k0 = (kt_begin + kt) * T::BK;
         const uint32_t st = base + s * T::STAGE;
         {
@@ -125,15 +140,16 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                 }
             }
 #pragma unroll
-            for (int j = 0; j < A_COPIES; ++j) {
+            for (int jj = 0; jj < A_COPIES / NG; ++jj) {
+                const int j = grp * (A_COPIES / NG) + jj;
                 const uint32_t dst =
-                    st + (VEC_A ? a_off0 + j * 2048 : ((j & 1) ? a_off1 : a_off0) + (j >> 1) * 1024);
-                const float *g = src + j * a_step;
+                    st + (VEC_A ? a_off0 + j * 2048 : ((jj & 1) ? a_off1 : a_off0) + (j >> 1) * 1024);
+                const float *g = src + (int64_t)j * a_step;
                 if constexpr (FULL) {
                     if constexpr (VEC_A) cp_async_16(dst, g, 16);
                     else cp_async_4(dst, g, 4);
                 } else {
-                    const int bytes = ((a_rows_ok >> j) & 1u) ? a_bytes : 0;
+                    const int bytes = m0c + a_row0 + j * A_ROW_STEP < M ? a_bytes : 0;
                     const void *gg = bytes ? (const void *)g : (const void *)A;
                     if constexpr (VEC_A) cp_async_16(dst, gg, bytes);
                     else cp_async_4(dst, gg, bytes);
@@ -143,12 +159,13 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         {
             const float *src = gB + (int64_t)k0 * ldb;
 #pragma unroll
-            for (int j = 0; j < B_COPIES; ++j) {
+            for (int jj = 0; jj < B_COPIES / NG; ++jj) {
+                const int j = grp * (B_COPIES / NG) + jj;
                 const uint32_t dst = st + b_off0 + j * B_KROW_STEP * (T::BN * 4);
-                const float *g = src + j * b_step;
+                const float *g = src + (int64_t)j * b_step;
                 if constexpr (FULL) {
-                    if constexpr (VEC_B) cp_async_16(dst, g, 16);
-                    else cp_async_4(dst, g, 4);
+                    if constexpr (VEC_B) cp_async_16(dst, g, b_bytes);
+                    else cp_async_4(dst, g, b_bytes);
                 } else {
                     const int kr = b_krow0 + j * B_KROW_STEP;
                     const int bytes = k0 + kr < K ? b_bytes : 0;
@@ -159,9 +176,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
             }
         }
     };
+    // steps 0 .. kt_full - 1 are FULL
+    const int kt_full = shift_m ? min(KT, K / T::BK - kt_begin) : 0;
+    auto full_step = [&](int kt) { return kt < kt_full; };
     auto issue = [&](int kt, int s) {
-        if (full_mn && (kt_begin + kt + 1) * T::BK <= K) issue_impl(std::true_type{}, kt, s);
-        else issue_impl(std::false_type{}, kt, s);
+        if (full_step(kt)) issue_impl(std::true_type{}, std::integral_constant<int, 1>{}, kt, s, 0);
+        else issue_impl(std::false_type{}, std::integral_constant<int, 1>{}, kt, s, 0);
     };
 
     // ---------------------------------------------------------------- compute roles (as the TMA kernel)
@@ -188,13 +208,23 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % T::STAGES;
         // step kt has landed for this thread; the barrier makes it every thread's,
-        // and frees the stage read in step kt - 1 for the copy issued below
+        // and frees the stage read in step kt - 1 for the copies issued below
         cp_async_wait<T::STAGES - 2>();
         __syncthreads();
         const int next = kt + T::STAGES - 1;
-        if (next < KT) issue(next, next % T::STAGES);
+        const int sn = next % T::STAGES;
+        const unsigned char *sa = smem + s * T::STAGE + row0 * 128;
+        const unsigned char *sb = smem + s * T::STAGE + T::A_STAGE + col0 * 4;
+        if (SPREAD && next < KT && full_step(next)) {
+            // the copies of step `next`, an eighth before each group of four k
+            tile_fma<T>(acc, acc2, sa, sb, lm, [&](int g) {
+                issue_impl(std::true_type{}, std::integral_constant<int, 8>{}, next, sn, g);
+            });
+        } else {
+            if (next < KT) issue(next, sn);
+            tile_fma<T>(acc, acc2, sa, sb, lm);
+        }
         cp_async_commit();
-        tile_fma<T>(acc, acc2, smem + s * T::STAGE + row0 * 128, smem + s * T::STAGE + T::A_STAGE + col0 * 4, lm);
     }
     // no copy in flight, every warp done with the stage buffers
     cp_async_wait<0>();
@@ -206,8 +236,9 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
             return;
         }
     }
-    if (vec_c) store_tile<T, true, CSPLIT>(acc, acc2, C, ldc, M, N, m0 + row0, n0 + col0, alpha, beta, cs, rank);
-    else store_tile<T, false, CSPLIT>(acc, acc2, C, ldc, M, N, m0 + row0, n0 + col0, alpha, beta, cs, rank);
+    // rows m0c .. m0 - 1 of a moved-up tile belong to the tile above
+    if (vec_c) store_tile<T, true, CSPLIT>(acc, acc2, C, ldc, M, N, m0c + row0, n0 + col0, alpha, beta, cs, rank, m0);
+    else store_tile<T, false, CSPLIT>(acc, acc2, C, ldc, M, N, m0c + row0, n0 + col0, alpha, beta, cs, rank, m0);
     if constexpr (CSPLIT) griddep_wait();
 }
 

@@ -113,16 +113,24 @@ enum : int { kDeviceErrNone = 0, kDeviceErrTimeout = 1 };
 // bounded waits run out.
 enum : int { kDebugSkipCopies = 1 };
 
+// A tile_fma hook that does nothing.
+struct NoHook {
+    __device__ __forceinline__ void operator()(int) const {}
+};
+
 // One pipeline stage of the outer-product FMAs: BK k-values for this thread's
 // TM x TN block of C, reading its A rows at `sa` (128-byte rows with the
 // 128-byte swizzle: the thread's rows are lm + 8 i) and its B row segments at
-// `sb`.
-template <class T>
+// `sb`.  hook(g) runs before each group g of four k-values, so a caller can
+// spread other work (copies for a later stage) through the FMAs.
+template <class T, class Hook = NoHook>
 __device__ __forceinline__ void tile_fma(float (&acc)[T::PACKED ? 1 : T::TM][T::PACKED ? 1 : T::TN],
                                          uint64_t (&acc2)[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1],
-                                         const unsigned char *sa, const unsigned char *sb, int lm) {
+                                         const unsigned char *sa, const unsigned char *sb, int lm,
+                                         Hook hook = Hook{}) {
 #pragma unroll T::G_UNROLL
     for (int g = 0; g < T::BK / 4; ++g) {
+        hook(g);
         // four k-values for each of the 8 rows, from the swizzled chunk g ^ lm
         const unsigned char *ag = sa + ((g ^ lm) << 4);
         float4 a[T::TM];
@@ -260,17 +268,18 @@ __device__ __forceinline__ bool cluster_reduce(uint64_t (&acc2)[T::PACKED ? T::T
 }
 
 // Epilogue: this thread's rows r0 + 8 i and 16-byte column quads at c0 + 16 q
-// (matrix coordinates); C = alpha * acc + beta * C, masked at the edges.  With
-// the cluster split, only the rows this rank added up.
+// (matrix coordinates); C = alpha * acc + beta * C, masked at the edges: rows
+// below row_lo or from M on, and columns from N on, are not stored.  With the
+// cluster split, only the rows this rank added up.
 template <class T, bool VEC_C, bool CSPLIT>
 __device__ __forceinline__ void store_tile(const float (&acc)[T::PACKED ? 1 : T::TM][T::PACKED ? 1 : T::TN],
                                            const uint64_t (&acc2)[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1],
                                            float *C, int ldc, int M, int N, int r0, int c0, float alpha, float beta,
-                                           int cs, int rank) {
+                                           int cs, int rank, int row_lo = 0) {
 #pragma unroll
     for (int i = 0; i < T::TM; ++i) {
         const int row = r0 + 8 * i;
-        if (row >= M) continue;
+        if (row >= M || row < row_lo) continue;
         if (CSPLIT && (i * cs) / T::TM != rank) continue;
         float *crow = C + (int64_t)row * ldc;
 #pragma unroll

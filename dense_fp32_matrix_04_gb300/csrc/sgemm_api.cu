@@ -140,6 +140,15 @@ bool use_tma(const Problem &p) {
 
 int k_tiles(const Problem &p) { return (p.K + TmaTile::BK - 1) / TmaTile::BK; }
 
+// The cp.async kernel holds its per-copy row strides in 32-bit registers: 16
+// rows of A (16-byte copies) or 4 (4-byte copies), 4 rows of B (16-byte) or 1.
+// An operand whose stride would not fit takes the narrower copies; A with
+// 4 * lda >= 2^31 (rows more than 2 GiB apart) cannot take that kernel at all.
+constexpr int64_t kIntMax = 0x7fffffff;
+bool cp_vec_a(const Problem &p) { return aligned16(p.A) && p.lda % 4 == 0 && 16 * (int64_t)p.lda <= kIntMax; }
+bool cp_vec_b(const Problem &p) { return aligned16(p.B) && p.ldb % 4 == 0 && 4 * (int64_t)p.ldb <= kIntMax; }
+bool cp_fits(const Problem &p) { return 4 * (int64_t)p.lda <= kIntMax; }
+
 template <class T, bool VC, int ROLE>
 bool tma_attr(int dev) {
     static std::atomic<int> done[kMaxDevices];
@@ -331,8 +340,8 @@ bool cp_packed_kernel(bool va, bool vb, int dev,
 template <class T>
 int launch_cp(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
               int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
-    const bool va = aligned16(p.A) && p.lda % 4 == 0;
-    const bool vb = aligned16(p.B) && p.ldb % 4 == 0;
+    const bool va = cp_vec_a(p);
+    const bool vb = cp_vec_b(p);
     const int dbg = g_debug_flags.load();
     void (*kernel)(int, int, int, float, const float *, int, const float *, int, float, float *, int, int, float *,
                    int, int) = nullptr;
@@ -364,6 +373,15 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     // partial slabs hold the raw products; alpha and beta act in the reduction
     const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
     const bool tma = use_tma(p);
+    if (!tma && !cp_fits(p)) {
+        // rows of A more than 2 GiB apart and not 16-byte aligned: the register-
+        // tiled kernel of the pages' ladder, which indexes in 64 bits (C = A B;
+        // the entry points that get here pass alpha = 1, beta = 0, one split)
+        if (splits != 1 || p.alpha != 1.f || p.beta != 0.f || (p.M + 63) / 64 > 65535) return SGEMM_ERR_INVALID_ARG;
+        sgemm::ladder_register_kernel<64, 64, 8, 4, 4><<<dim3((p.N + 63) / 64, (p.M + 63) / 64), 256, 0, stream>>>(
+            p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc);
+        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
     if (tma && splits == 1 && p.K <= 2 * TmaSmallK::BK) {
         const int64_t tiles =
             (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
@@ -636,6 +654,7 @@ int sgemm_f32_splitk(int M, int N, int K, const float *A, int lda, const float *
     // more splits than k-steps would leave empty slabs: cap at the k-step count
     const int kt = k_tiles(p);
     if (splits > kt) splits = kt > 0 ? kt : 1;
+    if (!use_tma(p) && !cp_fits(p)) splits = 1;
     if (splits > 1) {
         const size_t need = partials_bytes(M, N, splits);
         if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
@@ -666,6 +685,7 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const
     if ((int64_t)M * N == 0) return SGEMM_OK;
     const int kt = k_tiles(p);
     if (splits > kt) splits = kt > 0 ? kt : 1;
+    if (!use_tma(p) && !cp_fits(p)) splits = 1;
     const int ldp = ld_partials(N);
     if (splits > 1 && (long long)splits * M * ldp > kNoallocScratchFloats) return SGEMM_ERR_SCRATCH_LIMIT;
     DeviceInfo info;

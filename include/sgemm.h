@@ -70,8 +70,15 @@ typedef enum {
  *     accelerator (TMA) with hardware zero-fill at the edges, 8 x 16 outputs
  *     per thread accumulated with packed two-wide FP32 FMAs;
  *   - otherwise (and for K == 0): the same tiles, fragment reads and packed
- *     FMAs, fed by cp.async copies with per-element masks (16-byte copies for
- *     an operand whose rows are 16-byte aligned, 4-byte copies otherwise).
+ *     FMAs, fed by cp.async copies (16-byte copies for an operand whose rows
+ *     are 16-byte aligned, 4-byte copies otherwise).  A last, partial row of
+ *     tiles reads the 128 rows of A that end at row M and stores only its
+ *     own; B's right edge is a per-thread copy size; only the last, partial
+ *     k-step and products with M < 128 take per-element masks.  The copy
+ *     strides are 32-bit: an operand needing 16 * lda (A) or 4 * ldb (B)
+ *     >= 2^31 takes 4-byte copies, and an A whose rows are not 16-byte
+ *     aligned with 4 * lda >= 2^31 is computed by the pages' register-tiled
+ *     ladder kernel (64-bit indexing, much slower).
  * On both paths, when a grid would leave SMs idle (few tiles, or a last
  * partial round of tiles over the SMs), those tiles are each shared by a
  * thread-block cluster of 2, 4 or 8 blocks that split its k-steps and add their

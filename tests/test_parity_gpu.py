@@ -7,6 +7,7 @@ import pytest
 
 import gen
 from helpers import check_entries, check_full, check_rows, run_sgemm
+from oracle import ref_gemm
 
 pytestmark = pytest.mark.gpu
 
@@ -203,3 +204,41 @@ def test_matmul_wrapper_strided_views(sg):
     out = sg.matmul(bigA[:, :80], torch.from_numpy(B).cuda())
     torch.cuda.synchronize()
     check_full(out.cpu().numpy(), A, B)
+
+
+@pytest.mark.parametrize("case", ["a_rows_beyond_2gib", "a_vec_stride_demoted", "b_vec_stride_demoted"])
+def test_strides_beyond_32_bits(sg, case):
+    # the cp.async kernel keeps its copy strides in 32 bits: 16-byte copies of A
+    # step 16 rows, of B 4 rows.  16 * lda >= 2^31 or 4 * ldb >= 2^31 must fall
+    # back to 4-byte copies, and an unaligned A with 4 * lda >= 2^31 to the
+    # 64-bit ladder kernel -- each still the exact product
+    import torch
+    M, N, K = 3, 5, 7
+    if case == "a_rows_beyond_2gib":
+        lda, ldb = (1 << 29) + 1, N              # unaligned A, 4 * lda > 2^31
+    elif case == "a_vec_stride_demoted":
+        lda, ldb = (1 << 27) + 4, N + 1          # aligned A with 16 * lda > 2^31; B unaligned
+        M, K = 2, 64
+    else:
+        lda, ldb = K + 1, (1 << 29) + 4          # aligned B with 4 * ldb > 2^31; A unaligned
+        K = 2
+    A, B = gen.operands(M, N, K, seed=12, integer_copy=True)
+    dA = torch.zeros((M - 1) * lda + K, device="cuda")
+    dB = torch.zeros((K - 1) * ldb + N, device="cuda")
+    for r in range(M):
+        dA[r * lda: r * lda + K] = torch.from_numpy(A[r]).cuda()
+    for r in range(K):
+        dB[r * ldb: r * ldb + N] = torch.from_numpy(B[r]).cuda()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    sg.sgemm_f32(M, N, K, dA, lda, dB, ldb, C, N)
+    torch.cuda.synchronize()
+    C64, _ = ref_gemm.gemm_f64(A, B)
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), C64)
+    # one split where the cp.async kernel cannot run; the product is still exact
+    need = sg.sgemm_f32_splitk_workspace_size(M, N, 2)
+    ws = torch.empty(max(need // 4, 4), device="cuda")
+    C2 = torch.full((M, N), float("nan"), device="cuda")
+    sg.sgemm_f32_splitk(M, N, K, dA, lda, dB, ldb, C2, N, 2, ws, need)
+    torch.cuda.synchronize()
+    assert np.array_equal(C2.cpu().numpy().astype(np.float64), C64)
+    del dA, dB
