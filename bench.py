@@ -57,6 +57,7 @@ TRAFFIC_PROFILES = {
     "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES),
     "ragged_3001x4999x2047": ("ffma_cp_ragged_3001x4999x2047.md",
                               ["dense_fp32_matrix_04_gb300/csrc/ffma_cp_packed.cuh"] + KERNEL_SOURCES),
+    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES),
 }
 
 
@@ -326,7 +327,7 @@ def kernel_name(sg, M, N, K):
     if K > 0 and K % 4 == 0 and N % 4 == 0:
         if K <= 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed small-K tile, 1 stage, 8x8 per thread as "
-                    "fma.rn.f32x2 column pairs, 3 CTAs/SM)")
+                    "fma.rn.f32x2 column pairs, 4 CTAs/SM)")
         name = ("sgemm_ffma_tma_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as fma.rn.f32x2 "
                 "column pairs, 2 CTAs/SM)")
         tiles, full, cs = sg.sgemm_f32_plan(M, N, K)

@@ -99,12 +99,14 @@ using TmaMainTile = TmaTile<8, 16, 2, 2, 3, 1, 2, 4, true>;
 
 // Products with one or two k-steps (K <= 64, e.g. 16384 x 16384 x 32), where
 // each block loads once, computes briefly and spends most of its time storing
-// C: 128 x 64 tiles, 8 x 8 packed per thread, a single stage and 3 blocks per
-// SM (138 registers, no spills) so that the blocks of an SM overlap each
-// other's loads, FFMAs and stores.  Measured at 16384 x 16384 x 32: 0.375 ms
-// per product in the benchmark's timed loop against 0.379 ms for the main
-// configuration (0.389 against 0.445 ms in a tight launch loop).
-using TmaSmallKTile = TmaTile<8, 8, 2, 2, 1, 1, 3, 4, true>;
+// C: 128 x 64 tiles, 8 x 8 packed per thread, a single stage and 4 blocks per
+// SM (128 registers, no spills) so that the blocks of an SM overlap each
+// other's loads, FFMAs and stores; row-outer order with the eight groups of
+// four k unrolled (the column-pair-outer order spills at this register
+// count).  Measured at 16384 x 16384 x 32: 0.355 ms per product against
+// 0.370 ms with 3 blocks per SM (138 registers) and 0.379 ms for the main
+// configuration; at K = 64, 0.616 against 0.685 ms.
+using TmaSmallKTile = TmaTile<8, 8, 2, 2, 1, 0, 4, 8, true>;
 
 // Error codes written to the device error word.
 enum : int { kDeviceErrNone = 0, kDeviceErrTimeout = 1 };
