@@ -295,7 +295,7 @@ def f32_launches(sg, M, N, K):
     """Kernels one sgemm_f32 call launches: one, or two when a cluster-split
     grid follows whole rounds of plain tiles (sgemm_f32_plan)."""
     if K > 0 and M * N > 0:
-        tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
+        tiles, full, cs, _ = sg.sgemm_f32_plan(M, N, K)
         return 2 if cs > 1 and 0 < full < tiles else 1
     return 1
 
@@ -328,16 +328,20 @@ def kernel_name(sg, M, N, K):
         if K <= 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed small-K tile, 1 stage, 8x8 per thread as "
                     "fma.rn.f32x2 column pairs, 4 CTAs/SM)")
+        tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
+        if tn == 64:
+            return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed narrow tile, 2 stages, 8x8 per thread as "
+                    f"fma.rn.f32x2 column pairs, 4 CTAs/SM); all {tiles} tiles split over {cs}-CTA clusters "
+                    "(k-steps divided, partial sums added through distributed shared memory)")
         name = ("sgemm_ffma_tma_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as fma.rn.f32x2 "
                 "column pairs, 2 CTAs/SM)")
-        tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
         if cs > 1:
             name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                      "added through distributed shared memory)")
         return name
     name = ("sgemm_ffma_cp_kernel (128x128x32 tile fed by cp.async, 3 stages, 8x16 per thread as fma.rn.f32x2 "
             "column pairs, 2 CTAs/SM)")
-    tiles, full, cs = sg.sgemm_f32_plan(M, N, K) if K > 64 else (0, 0, 1)
+    tiles, full, cs, _ = sg.sgemm_f32_plan(M, N, K, aligned=False) if K > 0 else (0, 0, 1, 128)
     if cs > 1:
         name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                  "added through distributed shared memory)")

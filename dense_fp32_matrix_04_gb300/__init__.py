@@ -47,8 +47,9 @@ _SIGNATURES = {
     "sgemm_f32": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
-    "sgemm_f32_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
-                                      ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_int)]),
+    "sgemm_f32_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
+                                      ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "sgemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "sgemm_version": (ctypes.c_int, []),
     "sgemm_f32_splitk": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -206,14 +207,15 @@ def sgemm_f32_splitk_workspace_size(M: int, N: int, splits: int) -> int:
     return int(load().sgemm_f32_splitk_workspace_size(int(M), int(N), int(splits)))
 
 
-def sgemm_f32_plan(M: int, N: int, K: int):
-    """(tiles, full_tiles, cluster_size): how sgemm_f32 launches an aligned
-    M x N x K product on the current device.  Tiles past full_tiles are split
+def sgemm_f32_plan(M: int, N: int, K: int, aligned: bool = True):
+    """(tiles, full_tiles, cluster_size, tile_n): how sgemm_f32 launches an
+    M x N x K product on the current device, for operands the TMA can address
+    (aligned) or not.  Tiles are 128 x tile_n; tiles past full_tiles are split
     over thread-block clusters of cluster_size blocks (1: no split)."""
-    t, f, c = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_int(0)
-    _check(load().sgemm_f32_plan(int(M), int(N), int(K), ctypes.byref(t), ctypes.byref(f), ctypes.byref(c)),
-           "sgemm_f32_plan")
-    return int(t.value), int(f.value), int(c.value)
+    t, f, c, n = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().sgemm_f32_plan(int(M), int(N), int(K), 1 if aligned else 0, ctypes.byref(t), ctypes.byref(f),
+                                 ctypes.byref(c), ctypes.byref(n)), "sgemm_f32_plan")
+    return int(t.value), int(f.value), int(c.value), int(n.value)
 
 
 def sgemm_f32_splitk_suggest(M: int, N: int, K: int) -> int:

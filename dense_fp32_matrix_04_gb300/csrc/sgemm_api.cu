@@ -31,6 +31,7 @@ namespace {
 
 using TmaTile = sgemm::TmaMainTile;
 using TmaSmallK = sgemm::TmaSmallKTile;
+using TmaNarrow = sgemm::TmaNarrowTile;
 using X3Tile = sgemm::Tf32x3MainTile;
 
 constexpr int kMaxDevices = 64;
@@ -38,14 +39,15 @@ constexpr int kMaxSplits = 64;
 
 // test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernels.
 // Bit 1: route every product to the cp.async-fed kernel.  Bits 4..7: cluster
-// size forced on the cluster split (0 = the automatic plan, 1 = never split,
-// 2 .. 8 = split the tiles beyond whole multiples of the SM count with that
-// cluster size); bit 8: put every tile in the cluster-split launch; bit 9: no
-// programmatic overlap.
+// size forced on the cluster split of the main tile (0 = the automatic plan,
+// 1 = never split, 2 .. 8 = split the tiles beyond whole multiples of the SM
+// count with that cluster size); bit 8: put every tile in the cluster-split
+// launch; bit 9: no programmatic overlap; bit 10: never use the narrow tile.
 constexpr int kDebugForceCpAsync = 2;
 constexpr int kDebugClusterShift = 4;
 constexpr int kDebugClusterAll = 256;
 constexpr int kDebugNoOverlap = 512;  // launch the cluster-split grid without programmatic overlap
+constexpr int kDebugNoNarrow = 1024;
 std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
@@ -208,6 +210,7 @@ struct SplitPlan {
     int64_t tiles = 0;
     int64_t full = 0;
     int cs = 1;
+    bool narrow = false;  // tiles are the narrow tile's (128 x 64), all of them in clusters of cs
 };
 
 // Cost model of the main tile, fitted to measurements on GB300 of products from
@@ -224,12 +227,31 @@ double sm_time(int64_t L, double w) {
     return (double)(L / 2) * (w + kCtaOverheadSteps) + (double)(L % 2) * (0.5 * w + kCtaOverheadSteps);
 }
 
+// Cost model of the narrow tile in the same units, fitted to 17 products on
+// GB300 (512^3 to 2048 x 2048 x 512, each with fewer main tiles than SMs): an
+// SM advances kNarrowStepsPerUnit of its CTAs' k-steps (each half a main
+// k-step of work) per unit while two or more of them are resident, half as
+// many with one alone, and spends kNarrowRoundOverhead per round of up to four
+// CTAs.  Over those products the plan it picks ran within 6 % of the fastest
+// of the main plan and clusters of 2, 4 and 8 narrow CTAs.
+constexpr double kNarrowStepsPerUnit = 4.3;
+constexpr double kNarrowRoundOverhead = 1.25;
+
+// Time for an SM to run L narrow CTAs of w k-steps each.
+double narrow_sm_time(int64_t L, double w) {
+    if (L <= 1) return w / (0.5 * kNarrowStepsPerUnit) + kNarrowRoundOverhead;
+    return (double)L * w / kNarrowStepsPerUnit + kNarrowRoundOverhead * (double)((L + 3) / 4);
+}
+
 // The cluster split fills SMs that a grid would leave idle.  With P SMs, the
 // `rem` tiles beyond whole multiples of P (all of them when there are fewer
 // than P) are shared by clusters of c = 2, 4 or 8 CTAs -- c chosen by the cost
 // model among those leaving at least four 32-deep k-steps per CTA, ties to the
-// larger c -- when the estimate beats the plain grid by 4 % or more.
-SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info) {
+// larger c -- when the estimate beats the plain grid by 4 % or more.  With
+// fewer main tiles than SMs and operands the TMA can address (`narrow_ok`),
+// the narrow tile in clusters of 2, 4 or 8 (the c with the lowest estimate,
+// ties to the larger c) is taken instead when its estimate is lower still.
+SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, bool narrow_ok) {
     using T = TmaTile;
     SplitPlan plan;
     plan.tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
@@ -252,7 +274,24 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info) {
             const double t = sm_time(full / P, (double)kt) + sm_time((rem * c + P - 1) / P, (double)((kt + c - 1) / c));
             if (t <= best) best = t, cs = c;
         }
-        if (cs > 1 && best > 0.96 * plain) cs = 1;
+        if (cs > 1 && best > 0.96 * plain) cs = 1, best = plain;
+        if (narrow_ok && !(dbg & kDebugNoNarrow) && plan.tiles < P) {
+            using TN = TmaNarrow;
+            const int64_t ntiles = (int64_t)((M + TN::BM - 1) / TN::BM) * ((N + TN::BN - 1) / TN::BN);
+            int ncs = 0;
+            double nbest = 0.0;
+            for (int c = 2; c <= 8 && kt >= 4 * c; c *= 2) {
+                const double t = narrow_sm_time((ntiles * c + P - 1) / P, (double)((kt + c - 1) / c));
+                if ((ncs == 0 || t <= nbest) && cluster_fits<TN>(info.dev, c)) nbest = t, ncs = c;
+            }
+            if (ncs > 0 && nbest < best) {
+                plan.tiles = ntiles;
+                plan.full = 0;
+                plan.cs = ncs;
+                plan.narrow = true;
+                return plan;
+            }
+        }
     }
     if (cs < 2 || cs > 8 || full == plan.tiles) return plan;
     if (!cluster_fits<T>(info.dev, cs)) return plan;
@@ -396,7 +435,9 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
         const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
         return launch(0, tiles, splits, 1, false);
     }
-    const SplitPlan plan = split_plan(p.M, p.N, p.K, info);
+    const SplitPlan plan = split_plan(p.M, p.N, p.K, info, tma);
+    if (plan.narrow)
+        return launch_tma<TmaNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false, stream, info);
     if (plan.full > 0) {
         const int st = launch(0, plan.full, 1, 1, plan.cs > 1);
         if (st != SGEMM_OK || plan.full == plan.tiles) return st;
@@ -594,7 +635,7 @@ const char *sgemm_status_string(int status) {
     }
 }
 
-int sgemm_version(void) { return 101; }
+int sgemm_version(void) { return 102; }
 
 int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
               cudaStream_t stream) {
@@ -606,22 +647,27 @@ int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int 
     return launch_product(p, 1, nullptr, 0, stream, info);
 }
 
-int sgemm_f32_plan(int M, int N, int K, long long *tiles, long long *full_tiles, int *cluster_size) {
-    if (!tiles || !full_tiles || !cluster_size || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long long *full_tiles, int *cluster_size,
+                   int *tile_n) {
+    if (!tiles || !full_tiles || !cluster_size || !tile_n || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
     *tiles = *full_tiles = 0;
     *cluster_size = 1;
+    *tile_n = TmaTile::BN;
     if ((int64_t)M * N == 0) return SGEMM_OK;
     DeviceInfo info;
     if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
-    if (K <= 2 * TmaSmallK::BK) {
+    const bool cp = !tma_operands || (g_debug_flags.load() & kDebugForceCpAsync) != 0;
+    if (K <= 2 * TmaSmallK::BK && K > 0 && !cp) {
         *tiles = *full_tiles =
             (long long)((M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((N + TmaSmallK::BN - 1) / TmaSmallK::BN);
+        *tile_n = TmaSmallK::BN;
         return SGEMM_OK;
     }
-    const SplitPlan plan = split_plan(M, N, K, info);
+    const SplitPlan plan = split_plan(M, N, K, info, K > 0 && !cp);
     *tiles = plan.tiles;
     *full_tiles = plan.full;
     *cluster_size = plan.cs;
+    *tile_n = plan.narrow ? TmaNarrow::BN : TmaTile::BN;
     return SGEMM_OK;
 }
 

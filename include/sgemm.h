@@ -83,8 +83,10 @@ typedef enum {
  * partial round of tiles over the SMs), those tiles are each shared by a
  * thread-block cluster of 2, 4 or 8 blocks that split its k-steps and add their
  * partial sums through distributed shared memory in a fixed rank order: no
- * workspace, and the same bits on every run (sgemm_f32_plan reports the
- * choice).
+ * workspace, and the same bits on every run.  With fewer 128 x 128 tiles than
+ * SMs, the TMA path may instead use narrow 128 x 64 tiles (8 x 8 outputs per
+ * thread, four blocks per SM), all in such clusters (sgemm_f32_plan reports
+ * the choice).
  * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
  * The TMA kernel's waits are bounded: if a copy never lands, its blocks give
  * up, write nothing, and the next sgemm_device_status() returns
@@ -97,17 +99,22 @@ int sgemm_f32(int M, int N, int K,
               cudaStream_t stream);
 
 /*
- * How sgemm_f32 launches an M x N x K product on the current device: *tiles =
- * the number of output tiles (128 x 128; 128 x 64 for aligned operands with
- * K <= 64, which are never split); the first *full_tiles of them run as a
- * plain grid, the rest as clusters of *cluster_size blocks that split each
- * tile's k-steps (*cluster_size == 1: no cluster split, *full_tiles ==
- * *tiles).  The result reflects the test-only switches of sgemm_debug_set.
- * Launches nothing.
+ * How sgemm_f32 launches an M x N x K product on the current device, for
+ * operands the TMA can address (tma_operands != 0: A, B 16-byte aligned with
+ * leading dimensions that are multiples of 4) or not (0): *tiles = the number
+ * of output tiles, 128 rows by *tile_n columns; the first *full_tiles of them
+ * run as a plain grid, the rest as clusters of *cluster_size blocks that
+ * split each tile's k-steps (*cluster_size == 1: no cluster split,
+ * *full_tiles == *tiles).  *tile_n is 64 for TMA operands with 1 <= K <= 64
+ * (never split) and for the narrow tile, which a product with fewer 128 x 128
+ * tiles than SMs takes when its cost model says so (then every tile is in a
+ * cluster); 128 otherwise.  The result reflects the test-only switches of
+ * sgemm_debug_set.  Launches nothing.
  * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
  * if the device cannot be queried.
  */
-int sgemm_f32_plan(int M, int N, int K, long long *tiles, long long *full_tiles, int *cluster_size);
+int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long long *full_tiles,
+                   int *cluster_size, int *tile_n);
 
 /*
  * Split-K form of sgemm_f32 for grids with fewer output tiles than the GPU has
@@ -351,7 +358,9 @@ int sgemm_device_status(cudaStream_t stream);
  * cluster split, forced (0 = automatic, 1 = never split, 2 .. 8 =
  * split the tiles beyond whole multiples of the SM count with that size);
  * bit 8: with a forced size, split every tile; bit 9: no programmatic overlap
- * of the cluster-split launch with the plain one before it.  wait_limit_ns:
+ * of the cluster-split launch with the plain one before it; bit 10: never
+ * use the narrow tile (a forced cluster size also keeps the 128 x 128 tile).
+ * wait_limit_ns:
  * the bound of each wait
  * (default 2 s).  Affects every
  * later launch in this process.  SGEMM_ERR_INVALID_ARG if flags < 0 or

@@ -19,7 +19,10 @@ pytestmark = pytest.mark.gpu
 NO_SPLIT = 1 << 4
 ALL_TILES = 256
 NO_OVERLAP = 512
+NO_NARROW = 1024
 OVERHEAD = 2.0       # k-steps a block spends outside its k-loop
+NARROW_STEPS = 4.3   # narrow k-steps an SM advances per unit with two or more blocks resident
+NARROW_ROUND = 1.25  # units per round of up to four narrow blocks
 
 
 def forced(cs, all_tiles=True):
@@ -39,14 +42,23 @@ def sm_time(L, w):
     return (L // 2) * (w + OVERHEAD) + (L % 2) * (0.5 * w + OVERHEAD)
 
 
-def expected_plan(M, N, K, sms):
-    """The automatic plan restated: the 128 x 128 tiles beyond whole multiples
-    of the SM count P (all of them when there are fewer than P) are split over
-    the cluster size c = 2, 4 or 8 that minimises the cost model (an SM runs
-    blocks two at a time, each advancing a k-step per unit, or one alone at two
-    per unit; each block spends OVERHEAD units outside its k-loop, hidden when
-    it has a partner), ties to the larger c, keeping four 32-deep k-steps per
-    block, if that beats the plain grid by 4 %."""
+def narrow_sm_time(L, w):
+    if L <= 1:
+        return w / (0.5 * NARROW_STEPS) + NARROW_ROUND
+    return L * w / NARROW_STEPS + NARROW_ROUND * -(-L // 4)
+
+
+def expected_plan(M, N, K, sms, narrow=True):
+    """The automatic plan restated, as (tiles, full, cluster size, tile width):
+    the 128 x 128 tiles beyond whole multiples of the SM count P (all of them
+    when there are fewer than P) are split over the cluster size c = 2, 4 or 8
+    that minimises the cost model (an SM runs blocks two at a time, each
+    advancing a k-step per unit, or one alone at two per unit; each block
+    spends OVERHEAD units outside its k-loop, hidden when it has a partner),
+    ties to the larger c, keeping four 32-deep k-steps per block, if that beats
+    the plain grid by 4 %.  With fewer tiles than P (and TMA operands), 128 x 64
+    narrow tiles in clusters of c = 2, 4 or 8 (the lowest estimate, ties to the
+    larger c; NARROW_STEPS, NARROW_ROUND) replace that when lower still."""
     P = sms
     tiles = -(-M // 128) * -(-N // 128)
     rem = tiles % P
@@ -63,8 +75,19 @@ def expected_plan(M, N, K, sms):
             if t <= best:
                 best, cs = t, c
         if cs > 1 and best > 0.96 * plain:
-            cs = 1
-    return (tiles, full if cs > 1 else tiles, cs)
+            cs, best = 1, plain
+        if narrow and tiles < P:
+            ntiles = -(-M // 128) * -(-N // 64)
+            ncs, nbest = 0, 0.0
+            for c in (2, 4, 8):
+                if kt < 4 * c:
+                    break
+                t = narrow_sm_time(-(-ntiles * c // P), -(-kt // c))
+                if ncs == 0 or t <= nbest:
+                    ncs, nbest = c, t
+            if ncs and nbest < best:
+                return (ntiles, 0, ncs, 64)
+    return (tiles, full if cs > 1 else tiles, cs, 128)
 
 
 @pytest.mark.parametrize("cs", [2, 3, 4, 6, 8])
@@ -73,8 +96,8 @@ def expected_plan(M, N, K, sms):
 def test_forced_split_matches_oracle(sg, cs, M, N, K, seed):
     A, B = gen.operands(M, N, K, seed=seed)
     sg.sgemm_debug_set(forced(cs))
-    tiles, full, c = sg.sgemm_f32_plan(M, N, K)
-    assert (full, c) == (0, cs)
+    tiles, full, c, tn = sg.sgemm_f32_plan(M, N, K)
+    assert (full, c, tn) == (0, cs, 128)
     check_full(run_sgemm(sg, A, B), A, B)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
 
@@ -116,9 +139,9 @@ def test_tail_split_after_full_waves(sg, overlap):
     tiles_m = sms // tiles_n + 1              # one tile per SM, then a short tail
     M, N, K = 128 * tiles_m - 37, 128 * tiles_n - 4, 1000   # N % 4 == 0: the TMA path
     A, B = gen.operands(M, N, K, seed=207)
-    tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
-    assert (tiles, full, cs) == expected_plan(M, N, K, sms)
-    assert cs > 1 and 0 < full < tiles
+    tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
+    assert (tiles, full, cs, tn) == expected_plan(M, N, K, sms)
+    assert cs > 1 and 0 < full < tiles and tn == 128
     C = run_sgemm(sg, A, B)
     rows = [0, 1, 127, 128, M - 129, M - 128, M - 2, M - 1] + list(np.random.default_rng(1).integers(0, M, 12))
     check_rows(C, A, B, rows)
@@ -131,6 +154,10 @@ def test_automatic_plan(sg, M, N, K):
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms)
+    # operands the TMA cannot address never take the narrow tile
+    assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow=False)
+    sg.sgemm_debug_set(NO_NARROW)
+    assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms, narrow=False)
 
 
 def test_square_1024_uses_clusters_and_matches(sg):
@@ -141,8 +168,8 @@ def test_square_1024_uses_clusters_and_matches(sg):
 
 def test_no_split_switch(sg):
     sg.sgemm_debug_set(NO_SPLIT)
-    tiles, full, cs = sg.sgemm_f32_plan(1024, 1024, 1024)
-    assert cs == 1 and full == tiles == 64
+    tiles, full, cs, tn = sg.sgemm_f32_plan(1024, 1024, 1024)
+    assert cs == 1 and full == tiles == 64 and tn == 128
 
 
 @pytest.mark.parametrize("cs", [2, 4])
@@ -168,7 +195,7 @@ def test_timeout_in_cluster_mode(sg):
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()
     sg.sgemm_debug_set(forced(4) | 1, 50_000_000)
-    assert sg.sgemm_f32_plan(M, N, K)[2] == 4
+    assert sg.sgemm_f32_plan(M, N, K)[2:] == (4, 128)
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
@@ -187,8 +214,8 @@ def test_timeout_with_plain_waves_and_tail(sg):
     tiles_m = sms // tiles_n + 1
     M, N, K = 128 * tiles_m, 128 * tiles_n, 1024
     sg.sgemm_debug_set(1, 50_000_000)
-    tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
-    assert cs > 1 and 0 < full < tiles
+    tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
+    assert cs > 1 and 0 < full < tiles and tn == 128
     dA = torch.zeros(M, K, device="cuda")
     dB = torch.zeros(K, N, device="cuda")
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()

@@ -42,7 +42,7 @@ def _buffers(torch, M, N, K, aligned):
 ])
 def test_sgemm_f32_replays_bitwise(sg, M, N, K, aligned, expect):
     import torch
-    tiles, full, cs = sg.sgemm_f32_plan(M, N, K)
+    tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K, aligned)
     if expect == "split":
         assert cs > 1 and full == 0
     if expect == "plain+split":

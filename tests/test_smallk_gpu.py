@@ -1,5 +1,5 @@
 """The small-K tile (K <= 64 on aligned operands: 128 x 64 tiles, one stage,
-three CTAs per SM) on large grids: against the FP64 oracle with ragged edges
+four CTAs per SM) on large grids: against the FP64 oracle with ragged edges
 and every K from 1 to 64 class, exactly on small integers, bit for bit against
 the main tile fed by cp.async (the same per-element arithmetic), with
 alpha/beta, and on the bounded-wait path with thousands of CTAs."""
