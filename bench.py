@@ -52,12 +52,15 @@ FP32_LANES_PER_SM = 128
 MAX_SM_MHZ = 2070.0
 KERNEL_SOURCES = ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_sgemm.cuh", "dense_fp32_matrix_04_gb300/csrc/ptx.cuh",
                   "dense_fp32_matrix_04_gb300/csrc/tile_map.cuh"]
-# workload -> (committed ncu summary with its DRAM bytes, kernel sources the capture covers)
+TILES = "dense_fp32_matrix_04_gb300/csrc/tiles.cuh"
+# workload -> (committed ncu summary with its DRAM bytes, kernel sources the
+# capture covers, the tile configuration in TILES it ran)
 TRAFFIC_PROFILES = {
-    "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES),
+    "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES, "TmaMainTile"),
     "ragged_3001x4999x2047": ("ffma_cp_ragged_3001x4999x2047.md",
-                              ["dense_fp32_matrix_04_gb300/csrc/ffma_cp_packed.cuh"] + KERNEL_SOURCES),
-    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES),
+                              ["dense_fp32_matrix_04_gb300/csrc/ffma_cp_packed.cuh"] + KERNEL_SOURCES, "TmaMainTile"),
+    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES, "TmaSmallKTile"),
+    "square_1024": ("ffma_narrow_square_1024.md", KERNEL_SOURCES, "TmaNarrowTile"),
 }
 
 
@@ -210,11 +213,19 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- ncu traffic
 
-def kernel_source_digest(sources=None):
+def kernel_source_digest(sources=None, tile=None):
+    """Digest of the kernel sources and, if named, the one line of TILES that
+    defines the tile configuration (so other configurations may change)."""
     h = hashlib.sha256()
     for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
+    if tile:
+        with open(os.path.join(ROOT, TILES)) as f:
+            lines = [l.strip() for l in f if l.strip().startswith(f"using {tile} =")]
+        if len(lines) != 1:
+            raise ValueError(f"{tile}: expected one definition in {TILES}")
+        h.update(lines[0].encode())
     return h.hexdigest()[:16]
 
 
@@ -223,14 +234,14 @@ def recorded_traffic(workload=DEFAULT_WORKLOAD):
     if the capture was taken on the kernel sources as they are now; else None."""
     if workload not in TRAFFIC_PROFILES:
         return None
-    name, sources = TRAFFIC_PROFILES[workload]
+    name, sources, tile = TRAFFIC_PROFILES[workload]
     try:
         text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
-    if not m or not d or d.group(1) != kernel_source_digest(sources):
+    if not m or not d or d.group(1) != kernel_source_digest(sources, tile):
         return None
     return int(m.group(1))
 

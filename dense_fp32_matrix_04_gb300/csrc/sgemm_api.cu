@@ -15,6 +15,7 @@
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
 #include "tf32x3_tcgen05.cuh"
+#include "tiles.cuh"
 
 // Device error word: kernels that give up on a bounded wait record a code here;
 // sgemm_device_status() reads and clears it.  One instance per device context.

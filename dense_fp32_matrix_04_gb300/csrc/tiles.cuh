@@ -1,0 +1,38 @@
+// The FFMA kernels' shipped tile configurations, one alias per line, each
+// with the measurements that chose it.
+#pragma once
+
+#include "ffma_tma_sgemm.cuh"
+
+namespace sgemm {
+
+// The shipped configuration: 128 x 128 block tile, 4 warps of 64 x 64, 8 x 16
+// outputs per thread accumulated as column pairs with fma.rn.f32x2 in
+// column-pair-outer order, 3 stages, k-groups unrolled by four, two CTAs per
+// SM.  Chosen by measurement at M = N = K = 8192 among scalar and packed
+// forms, per-thread tiles (8x8 .. 16x16), 128 to 512 threads, FFMA orders,
+// 2 to 4 stages and unroll depths: 82 % of the FP32 peak against 72 % for the
+// best scalar form (16 x 8, row-major order).
+using TmaMainTile = TmaTile<8, 16, 2, 2, 3, 1, 2, 4, true>;
+
+// Products with one or two k-steps (K <= 64, e.g. 16384 x 16384 x 32), where
+// each block loads once, computes briefly and spends most of its time storing
+// C: 128 x 64 tiles, 8 x 8 packed per thread, a single stage and 4 blocks per
+// SM (128 registers, no spills) so that the blocks of an SM overlap each
+// other's loads, FFMAs and stores; row-outer order with the eight groups of
+// four k unrolled (the column-pair-outer order spills at this register
+// count).  Measured at 16384 x 16384 x 32: 0.355 ms per product against
+// 0.370 ms with 3 blocks per SM (138 registers) and 0.379 ms for the main
+// configuration; at K = 64, 0.616 against 0.685 ms.
+using TmaSmallKTile = TmaTile<8, 8, 2, 2, 1, 0, 4, 8, true>;
+
+// Products with fewer 128 x 128 tiles than SMs (e.g. 1024^3, 2048 x 1024 x
+// 2048): 128 x 64 tiles, 8 x 8 packed per thread, 2 stages and 4 blocks per SM
+// (128 registers, no spills), always as thread-block clusters that split each
+// tile's k-steps.  Twice the tiles of the main configuration at twice the
+// blocks per SM spread the work over the SMs more evenly.  Measured (TFLOP/s,
+// against the main tile's plan): 1024^3 39.9 against 38.0, 2048 x 1024 x 2048
+// 54.4 against 47.6, 512^3 16.3 against 11.1.
+using TmaNarrowTile = TmaTile<8, 8, 2, 2, 2, 1, 4, 8, true>;
+
+}  // namespace sgemm

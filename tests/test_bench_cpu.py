@@ -52,9 +52,13 @@ def test_recorded_traffic_follows_the_kernel_sources():
     assert r is None or r > 4 * (3001 * 2047 + 2047 * 4999 + 3001 * 4999)
     assert bench.recorded_traffic("tiny_6x6x9") is None
     assert len(bench.kernel_source_digest()) == 16
-    for name, sources in bench.TRAFFIC_PROFILES.values():
+    for name, sources, tile in bench.TRAFFIC_PROFILES.values():
         assert os.path.exists(os.path.join(bench.ROOT, "profiles", name))
-        assert len(bench.kernel_source_digest(sources)) == 16
+        assert len(bench.kernel_source_digest(sources, tile)) == 16
+    # the digest names one tile configuration: another one's line does not enter it
+    d_main = bench.kernel_source_digest(bench.KERNEL_SOURCES, "TmaMainTile")
+    assert d_main != bench.kernel_source_digest(bench.KERNEL_SOURCES, "TmaNarrowTile")
+    assert d_main != bench.kernel_source_digest(bench.KERNEL_SOURCES)
 
 
 def test_tf32_peak_derivation():
