@@ -49,8 +49,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     // copy, so both loop bodies would be live in the SM's instruction cache),
     // measured faster in one burst.
     constexpr bool SPREAD = !VEC_A && ROLE != kRoleSplit;
-    static_assert(T::PACKED && T::THREADS == 128 && T::BM == 128 && T::BN == 128 && T::BK == 32,
-                  "the copy roles below are laid out for 128 threads and 128 x 128 x 32 tiles");
+    static_assert(T::PACKED && T::THREADS == 128 && T::BM == 128 && (T::BN == 128 || T::BN == 64) && T::BK == 32,
+                  "the copy roles below are laid out for 128 threads and 128 x 128 x 32 or 128 x 64 x 32 tiles");
     static_assert(T::STAGES >= 2, "the cp.async pipeline needs two stages");
     static_assert(!CSPLIT || T::CSPLIT_OK, "the cluster split exchanges packed accumulators through the stage buffers");
     if constexpr (ROLE == kRolePrimary) griddep_launch_dependents();
@@ -106,14 +106,18 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     // (j / 2) * 1024 (4-byte) or j * 2048 (16-byte) to the one of its parity
     auto a_off = [&](int r) { return (uint32_t)(r * 128 + ((((a_k >> 2) ^ (r & 7))) << 4) + (VEC_A ? 0 : (a_k & 3) * 4)); };
     const uint32_t a_off0 = a_off(a_row0), a_off1 = a_off(a_row0 + A_ROW_STEP);
-    // B, 4-byte: warp w copies columns 32 w + lane of k-rows j (j < 32).
-    // B, 16-byte: k-rows 4 j + w (j < 8), columns 4 lane .. 4 lane + 3.
+    // B, 4-byte: a warp copies 32 consecutive columns of one k-row per copy;
+    // the BN / 32 warps of a k-row (W) take columns 32 (w % W) + lane of k-rows
+    // w / W + (4 / W) j.  16-byte: a warp copies 32 / (BN / 4) k-rows of BN
+    // columns per copy, lane l taking the 16-byte chunk l % (BN / 4) of its row.
     // A thread's columns are the same in every k-step, so the right edge is a
     // per-thread copy size (zero past column N, from a column inside B).
-    constexpr int B_COPIES = VEC_B ? 8 : 32;
-    const int b_col = VEC_B ? 4 * lane : 32 * warp + lane;
-    const int b_krow0 = VEC_B ? warp : 0;
-    constexpr int B_KROW_STEP = VEC_B ? 4 : 1;
+    constexpr int B_WARPS_PER_ROW = T::BN / 32;
+    constexpr int B_CHUNKS_PER_ROW = T::BN / 4;
+    constexpr int B_KROW_STEP = VEC_B ? 4 * (32 / B_CHUNKS_PER_ROW) : 4 / B_WARPS_PER_ROW;
+    constexpr int B_COPIES = 32 / B_KROW_STEP;
+    const int b_col = VEC_B ? 4 * (lane % B_CHUNKS_PER_ROW) : 32 * (warp % B_WARPS_PER_ROW) + lane;
+    const int b_krow0 = VEC_B ? lane / B_CHUNKS_PER_ROW + (32 / B_CHUNKS_PER_ROW) * warp : warp / B_WARPS_PER_ROW;
     const int b_left = N - (n0 + b_col);
     const int b_bytes = VEC_B ? (b_left >= 4 ? 16 : (b_left > 0 ? 4 * b_left : 0)) : (b_left > 0 ? 4 : 0);
     const float *gB = B + (int64_t)b_krow0 * ldb + (b_left > 0 ? n0 + b_col : 0);
@@ -158,9 +162,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         }
         {
             const float *src = gB + (int64_t)k0 * ldb;
+            // with fewer copies than groups, group g < B_COPIES takes copy g
+            constexpr int BPG = B_COPIES >= NG ? B_COPIES / NG : 1;
 #pragma unroll
-            for (int jj = 0; jj < B_COPIES / NG; ++jj) {
-                const int j = grp * (B_COPIES / NG) + jj;
+            for (int jj = 0; jj < BPG; ++jj) {
+                const int j = grp * BPG + jj;
+                if (B_COPIES < NG && j >= B_COPIES) break;
                 const uint32_t dst = st + b_off0 + j * B_KROW_STEP * (T::BN * 4);
                 const float *g = src + (int64_t)j * b_step;
                 if constexpr (FULL) {

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/sgemm.h"
 #include "ffma_cp_packed.cuh"
@@ -33,6 +34,7 @@ namespace {
 using TmaTile = sgemm::TmaMainTile;
 using TmaSmallK = sgemm::TmaSmallKTile;
 using TmaNarrow = sgemm::TmaNarrowTile;
+using TmaNarrowCp = sgemm::TmaNarrowCpTile;
 using X3Tile = sgemm::Tf32x3MainTile;
 
 constexpr int kMaxDevices = 64;
@@ -151,6 +153,9 @@ constexpr int64_t kIntMax = 0x7fffffff;
 bool cp_vec_a(const Problem &p) { return aligned16(p.A) && p.lda % 4 == 0 && 16 * (int64_t)p.lda <= kIntMax; }
 bool cp_vec_b(const Problem &p) { return aligned16(p.B) && p.ldb % 4 == 0 && 4 * (int64_t)p.ldb <= kIntMax; }
 bool cp_fits(const Problem &p) { return 4 * (int64_t)p.lda <= kIntMax; }
+// The narrow tile's B copies step 8 rows (16-byte) or 2 (4-byte): it is used
+// only when every stride of either width fits.
+bool cp_narrow_fits(const Problem &p) { return 16 * (int64_t)p.lda <= kIntMax && 8 * (int64_t)p.ldb <= kIntMax; }
 
 template <class T, bool VC, int ROLE>
 bool tma_attr(int dev) {
@@ -182,21 +187,30 @@ cudaLaunchConfig_t split_config(int64_t clusters, int cs, bool overlap, cudaStre
 // Whether clusters of `cs` CTAs of the cluster-split kernel can be resident on
 // this device at all; queried once per device and size on the TMA form (the
 // cp.async form has the same block size, shared memory and CTAs per SM).
-template <class T>
+template <class T, bool VA, bool VB, int ROLE>
+bool cp_packed_attr(int dev);
+
+template <class T, bool CP = false>
 bool cluster_fits(int dev, int cs) {
     static std::atomic<int> known[kMaxDevices][9];  // 0 unknown, 1 yes, 2 no
     if (cs < 2 || cs > 8) return false;
     std::atomic<int> &slot = known[dev][cs];
     int k = slot.load(std::memory_order_acquire);
     if (k == 0) {
-        if (!tma_attr<T, true, sgemm::kRoleSplit>(dev)) return false;
+        bool smem_ok;
+        if constexpr (CP) smem_ok = cp_packed_attr<T, false, false, sgemm::kRoleSplit>(dev);
+        else smem_ok = tma_attr<T, true, sgemm::kRoleSplit>(dev);
+        if (!smem_ok) return false;
         cudaLaunchAttribute attr[2];
         const cudaLaunchConfig_t cfg = split_config<T>(1, cs, false, 0, attr);
         int n = 0;
-        const bool ok =
-            cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit>, &cfg) ==
-                cudaSuccess &&
-            n > 0;
+        cudaError_t e;
+        if constexpr (CP)
+            e = cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_cp_kernel<T, false, false, sgemm::kRoleSplit>,
+                                               &cfg);
+        else
+            e = cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit>, &cfg);
+        const bool ok = e == cudaSuccess && n > 0;
         if (!ok) (void)cudaGetLastError();
         k = ok ? 1 : 2;
         slot.store(k, std::memory_order_release);
@@ -228,31 +242,42 @@ double sm_time(int64_t L, double w) {
     return (double)(L / 2) * (w + kCtaOverheadSteps) + (double)(L % 2) * (0.5 * w + kCtaOverheadSteps);
 }
 
-// Cost model of the narrow tile in the same units, fitted to 17 products on
-// GB300 (512^3 to 2048 x 2048 x 512, each with fewer main tiles than SMs): an
-// SM advances kNarrowStepsPerUnit of its CTAs' k-steps (each half a main
-// k-step of work) per unit while two or more of them are resident, half as
-// many with one alone, and spends kNarrowRoundOverhead per round of up to four
-// CTAs.  Over those products the plan it picks ran within 6 % of the fastest
-// of the main plan and clusters of 2, 4 and 8 narrow CTAs.
-constexpr double kNarrowStepsPerUnit = 4.3;
-constexpr double kNarrowRoundOverhead = 1.25;
+// Cost model of the narrow tile in the same units (those of the main tile on
+// the same path): an SM advances `steps` of its CTAs' k-steps (each half a
+// main k-step of work) per unit while three or more of them are resident,
+// `two` times that with two, half with one alone, and spends `round` units per
+// round of up to `per_sm` CTAs.  Fitted on GB300 to products with fewer main
+// tiles than SMs: 17 of them from 512^3 to 2048 x 2048 x 512 for the TMA path,
+// 14 with lda = K + 1 (ldb = N + 1, or N + 4) for the cp.async path.  Over
+// those the plan it picks ran within 6 % (TMA) and 3 % (cp.async) of the
+// fastest of the main plan and clusters of 2, 4 and 8 narrow CTAs.
+struct NarrowModel {
+    double steps, two, round;
+    int per_sm;
+};
+constexpr NarrowModel kNarrowTma{4.4, 0.9, 1.25, 4};
+constexpr NarrowModel kNarrowCp{5.9, 0.75, 1.5, 3};
 
 // Time for an SM to run L narrow CTAs of w k-steps each.
-double narrow_sm_time(int64_t L, double w) {
-    if (L <= 1) return w / (0.5 * kNarrowStepsPerUnit) + kNarrowRoundOverhead;
-    return (double)L * w / kNarrowStepsPerUnit + kNarrowRoundOverhead * (double)((L + 3) / 4);
+double narrow_sm_time(const NarrowModel &m, int64_t L, double w) {
+    if (L <= 1) return w / (0.5 * m.steps) + m.round;
+    if (L == 2) return 2.0 * w / (m.two * m.steps) + m.round;
+    return (double)L * w / m.steps + m.round * (double)((L + m.per_sm - 1) / m.per_sm);
 }
+
+// Which narrow tile a product may take: none, the TMA kernel's, or the
+// cp.async kernel's.
+enum class Narrow { kNone, kTma, kCp };
 
 // The cluster split fills SMs that a grid would leave idle.  With P SMs, the
 // `rem` tiles beyond whole multiples of P (all of them when there are fewer
 // than P) are shared by clusters of c = 2, 4 or 8 CTAs -- c chosen by the cost
 // model among those leaving at least four 32-deep k-steps per CTA, ties to the
 // larger c -- when the estimate beats the plain grid by 4 % or more.  With
-// fewer main tiles than SMs and operands the TMA can address (`narrow_ok`),
-// the narrow tile in clusters of 2, 4 or 8 (the c with the lowest estimate,
-// ties to the larger c) is taken instead when its estimate is lower still.
-SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, bool narrow_ok) {
+// fewer main tiles than SMs, the narrow tile of the product's path (`narrow`)
+// in clusters of 2, 4 or 8 (the c with the lowest estimate, ties to the
+// larger c) is taken instead when its estimate is lower still.
+SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow) {
     using T = TmaTile;
     SplitPlan plan;
     plan.tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
@@ -276,14 +301,18 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, bool narrow_ok
             if (t <= best) best = t, cs = c;
         }
         if (cs > 1 && best > 0.96 * plain) cs = 1, best = plain;
-        if (narrow_ok && !(dbg & kDebugNoNarrow) && plan.tiles < P) {
+        if (narrow != Narrow::kNone && !(dbg & kDebugNoNarrow) && plan.tiles < P) {
+            static_assert(TmaNarrow::BM == TmaNarrowCp::BM && TmaNarrow::BN == TmaNarrowCp::BN, "one narrow tile shape");
             using TN = TmaNarrow;
+            const NarrowModel &m = narrow == Narrow::kTma ? kNarrowTma : kNarrowCp;
             const int64_t ntiles = (int64_t)((M + TN::BM - 1) / TN::BM) * ((N + TN::BN - 1) / TN::BN);
             int ncs = 0;
             double nbest = 0.0;
             for (int c = 2; c <= 8 && kt >= 4 * c; c *= 2) {
-                const double t = narrow_sm_time((ntiles * c + P - 1) / P, (double)((kt + c - 1) / c));
-                if ((ncs == 0 || t <= nbest) && cluster_fits<TN>(info.dev, c)) nbest = t, ncs = c;
+                const double t = narrow_sm_time(m, (ntiles * c + P - 1) / P, (double)((kt + c - 1) / c));
+                const bool fits = narrow == Narrow::kTma ? cluster_fits<TmaNarrow>(info.dev, c)
+                                                          : cluster_fits<TmaNarrowCp, true>(info.dev, c);
+                if ((ncs == 0 || t <= nbest) && fits) nbest = t, ncs = c;
             }
             if (ncs > 0 && nbest < best) {
                 plan.tiles = ntiles;
@@ -314,7 +343,11 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
     const unsigned long long wait = g_wait_limit_ns.load();
     const int dbg = g_debug_flags.load();
     using sgemm::sgemm_ffma_tma_kernel;
-    if (cs <= 1) {
+    // the narrow tiles only ever run as clusters
+    constexpr bool kClustersOnly = std::is_same_v<T, TmaNarrow> || std::is_same_v<T, TmaNarrowCp>;
+    if constexpr (kClustersOnly) {
+        if (cs <= 1) return SGEMM_ERR_LAUNCH;
+    } else if (cs <= 1) {
         const dim3 grid((unsigned)tiles, (unsigned)splits);
         if (primary) {
             if constexpr (!T::CSPLIT_OK) {
@@ -385,7 +418,10 @@ int launch_cp(const Problem &p, float alpha, float beta, bool vc, int splits, fl
     const int dbg = g_debug_flags.load();
     void (*kernel)(int, int, int, float, const float *, int, const float *, int, float, float *, int, int, float *,
                    int, int) = nullptr;
-    if (cs <= 1) {
+    constexpr bool kClustersOnly = std::is_same_v<T, TmaNarrow> || std::is_same_v<T, TmaNarrowCp>;
+    if constexpr (kClustersOnly) {
+        if (cs <= 1) return SGEMM_ERR_LAUNCH;
+    } else if (cs <= 1) {
         const bool attr = primary ? cp_packed_kernel<T, sgemm::kRolePrimary>(va, vb, info.dev, kernel)
                                   : cp_packed_kernel<T, sgemm::kRolePlain>(va, vb, info.dev, kernel);
         if (!attr) return SGEMM_ERR_LAUNCH;
@@ -436,9 +472,13 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
         const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
         return launch(0, tiles, splits, 1, false);
     }
-    const SplitPlan plan = split_plan(p.M, p.N, p.K, info, tma);
+    const Narrow narrow = tma ? Narrow::kTma : (cp_narrow_fits(p) ? Narrow::kCp : Narrow::kNone);
+    const SplitPlan plan = split_plan(p.M, p.N, p.K, info, narrow);
     if (plan.narrow)
-        return launch_tma<TmaNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false, stream, info);
+        return tma ? launch_tma<TmaNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false, stream,
+                                           info)
+                   : launch_cp<TmaNarrowCp>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false,
+                                            stream, info);
     if (plan.full > 0) {
         const int st = launch(0, plan.full, 1, 1, plan.cs > 1);
         if (st != SGEMM_OK || plan.full == plan.tiles) return st;
@@ -664,7 +704,7 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
         *tile_n = TmaSmallK::BN;
         return SGEMM_OK;
     }
-    const SplitPlan plan = split_plan(M, N, K, info, K > 0 && !cp);
+    const SplitPlan plan = split_plan(M, N, K, info, cp ? Narrow::kCp : Narrow::kTma);
     *tiles = plan.tiles;
     *full_tiles = plan.full;
     *cluster_size = plan.cs;

@@ -27,12 +27,20 @@ using TmaMainTile = TmaTile<8, 16, 2, 2, 3, 1, 2, 4, true>;
 using TmaSmallKTile = TmaTile<8, 8, 2, 2, 1, 0, 4, 8, true>;
 
 // Products with fewer 128 x 128 tiles than SMs (e.g. 1024^3, 2048 x 1024 x
-// 2048): 128 x 64 tiles, 8 x 8 packed per thread, 2 stages and 4 blocks per SM
+// 2048) on the TMA kernel: 128 x 64 tiles, 8 x 8 packed per thread, 2 stages and 4 blocks per SM
 // (128 registers, no spills), always as thread-block clusters that split each
 // tile's k-steps.  Twice the tiles of the main configuration at twice the
 // blocks per SM spread the work over the SMs more evenly.  Measured (TFLOP/s,
 // against the main tile's plan): 1024^3 39.9 against 38.0, 2048 x 1024 x 2048
 // 54.4 against 47.6, 512^3 16.3 against 11.1.
 using TmaNarrowTile = TmaTile<8, 8, 2, 2, 2, 1, 4, 8, true>;
+
+// The narrow tile of the cp.async-fed kernel (operands the TMA cannot
+// address): the same 128 x 64 tile and arithmetic with 3 stages and 3 blocks
+// per SM, since the copy addressing needs more than 128 registers (150-162,
+// no spills; at 4 blocks per SM it spills).  Measured with lda = K + 1 and
+// ldb = N + 1 (TFLOP/s, against the 128 x 128 cp.async plan): 2048 x 1024 x
+// 2048 44.6 against 32.6, 1536^3 43.6 against 35.4, 512^3 14.9 against 7.5.
+using TmaNarrowCpTile = TmaTile<8, 8, 2, 2, 3, 1, 3, 8, true>;
 
 }  // namespace sgemm

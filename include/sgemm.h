@@ -84,9 +84,10 @@ typedef enum {
  * thread-block cluster of 2, 4 or 8 blocks that split its k-steps and add their
  * partial sums through distributed shared memory in a fixed rank order: no
  * workspace, and the same bits on every run.  With fewer 128 x 128 tiles than
- * SMs, the TMA path may instead use narrow 128 x 64 tiles (8 x 8 outputs per
- * thread, four blocks per SM), all in such clusters (sgemm_f32_plan reports
- * the choice).
+ * SMs, either path may instead use narrow 128 x 64 tiles (8 x 8 outputs per
+ * thread; four blocks per SM on the TMA path, three on the cp.async path, the
+ * latter only when 16 * lda and 8 * ldb fit in 32 bits), all in such clusters
+ * (sgemm_f32_plan reports the choice).
  * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
  * The TMA kernel's waits are bounded: if a copy never lands, its blocks give
  * up, write nothing, and the next sgemm_device_status() returns
@@ -108,8 +109,9 @@ int sgemm_f32(int M, int N, int K,
  * *full_tiles == *tiles).  *tile_n is 64 for TMA operands with 1 <= K <= 64
  * (never split) and for the narrow tile, which a product with fewer 128 x 128
  * tiles than SMs takes when its cost model says so (then every tile is in a
- * cluster); 128 otherwise.  The result reflects the test-only switches of
- * sgemm_debug_set.  Launches nothing.
+ * cluster); 128 otherwise.  For non-TMA operands the plan assumes 16 * lda
+ * and 8 * ldb fit in 32 bits (otherwise the 128 x 128 plan runs).  The result
+ * reflects the test-only switches of sgemm_debug_set.  Launches nothing.
  * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
  * if the device cannot be queried.
  */

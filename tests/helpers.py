@@ -9,7 +9,7 @@ import numpy as np
 from oracle import ref_gemm, tolerance
 
 CANARY_BITS = np.int32(0x7FC0_1234)   # a quiet NaN with a payload no kernel produces
-GUARD = 67                            # guard words before and after each buffer
+GUARD = 64                            # guard words before and after each buffer (offset 0 stays 16-byte aligned)
 WS_GUARD = 64                         # guard words around a split-K workspace (keeps 16-byte alignment)
 
 

@@ -21,8 +21,10 @@ ALL_TILES = 256
 NO_OVERLAP = 512
 NO_NARROW = 1024
 OVERHEAD = 2.0       # k-steps a block spends outside its k-loop
-NARROW_STEPS = 4.3   # narrow k-steps an SM advances per unit with two or more blocks resident
-NARROW_ROUND = 1.25  # units per round of up to four narrow blocks
+# narrow-tile cost models, per path: (k-steps an SM advances per unit with
+# three or more blocks resident, the fraction of that with two, units per
+# round of blocks, blocks per SM)
+NARROW_MODEL = {"tma": (4.4, 0.9, 1.25, 4), "cp": (5.9, 0.75, 1.5, 3)}
 
 
 def forced(cs, all_tiles=True):
@@ -42,13 +44,16 @@ def sm_time(L, w):
     return (L // 2) * (w + OVERHEAD) + (L % 2) * (0.5 * w + OVERHEAD)
 
 
-def narrow_sm_time(L, w):
+def narrow_sm_time(model, L, w):
+    steps, two, rnd, per_sm = model
     if L <= 1:
-        return w / (0.5 * NARROW_STEPS) + NARROW_ROUND
-    return L * w / NARROW_STEPS + NARROW_ROUND * -(-L // 4)
+        return w / (0.5 * steps) + rnd
+    if L == 2:
+        return 2 * w / (two * steps) + rnd
+    return L * w / steps + rnd * -(-L // per_sm)
 
 
-def expected_plan(M, N, K, sms, narrow=True):
+def expected_plan(M, N, K, sms, narrow="tma"):
     """The automatic plan restated, as (tiles, full, cluster size, tile width):
     the 128 x 128 tiles beyond whole multiples of the SM count P (all of them
     when there are fewer than P) are split over the cluster size c = 2, 4 or 8
@@ -56,9 +61,10 @@ def expected_plan(M, N, K, sms, narrow=True):
     advancing a k-step per unit, or one alone at two per unit; each block
     spends OVERHEAD units outside its k-loop, hidden when it has a partner),
     ties to the larger c, keeping four 32-deep k-steps per block, if that beats
-    the plain grid by 4 %.  With fewer tiles than P (and TMA operands), 128 x 64
-    narrow tiles in clusters of c = 2, 4 or 8 (the lowest estimate, ties to the
-    larger c; NARROW_STEPS, NARROW_ROUND) replace that when lower still."""
+    the plain grid by 4 %.  With fewer tiles than P, 128 x 64 narrow tiles of
+    the path (`narrow`: "tma", "cp" or None) in clusters of c = 2, 4 or 8 (the
+    lowest estimate of that path's NARROW_MODEL, ties to the larger c) replace
+    that when lower still."""
     P = sms
     tiles = -(-M // 128) * -(-N // 128)
     rem = tiles % P
@@ -82,7 +88,7 @@ def expected_plan(M, N, K, sms, narrow=True):
             for c in (2, 4, 8):
                 if kt < 4 * c:
                     break
-                t = narrow_sm_time(-(-ntiles * c // P), -(-kt // c))
+                t = narrow_sm_time(NARROW_MODEL[narrow], -(-ntiles * c // P), -(-kt // c))
                 if ncs == 0 or t <= nbest:
                     ncs, nbest = c, t
             if ncs and nbest < best:
@@ -154,10 +160,11 @@ def test_automatic_plan(sg, M, N, K):
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms)
-    # operands the TMA cannot address never take the narrow tile
-    assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow=False)
+    # operands the TMA cannot address: the cp.async kernel's narrow tile and model
+    assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow="cp")
     sg.sgemm_debug_set(NO_NARROW)
-    assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms, narrow=False)
+    assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms, narrow=None)
+    assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow=None)
 
 
 def test_square_1024_uses_clusters_and_matches(sg):

@@ -1,10 +1,11 @@
-"""The narrow tile (128 x 64 tiles, 8 x 8 packed per thread, 2 stages, four
-CTAs per SM, every tile split over a thread-block cluster), which sgemm_f32
-takes for TMA operands when a product has fewer 128 x 128 tiles than SMs and
-the plan's cost model prefers it: against the FP64 oracle with ragged edges
-and a partial last k-step, exactly on small integers, bit for bit from run to
-run, with alpha/beta, within the bound of the 128 x 128 tile's result, and on
-the bounded-wait path (no fault, no hang)."""
+"""The narrow tiles (128 x 64 tiles, 8 x 8 packed per thread, every tile split
+over a thread-block cluster; 2 stages and four CTAs per SM on the TMA kernel,
+3 stages and three on the cp.async kernel), which sgemm_f32 takes when a
+product has fewer 128 x 128 tiles than SMs and the plan's cost model prefers
+them: against the FP64 oracle with ragged edges and a partial last k-step, on
+both kernels with every copy width, exactly on small integers, bit for bit
+from run to run, with alpha/beta, within the bound of the 128 x 128 tile's
+result, and on the bounded-wait path (no fault, no hang)."""
 
 import numpy as np
 import pytest
@@ -30,8 +31,8 @@ def ld4(n):
     return (n + 3) // 4 * 4
 
 
-def narrow_plan(sg, M, N, K):
-    tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
+def narrow_plan(sg, M, N, K, aligned=True):
+    tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K, aligned)
     assert tn == 64 and full == 0 and cs in (2, 4, 8), (M, N, K, tiles, full, cs, tn)
     assert tiles == -(-M // 128) * -(-N // 64)
     return cs
@@ -118,3 +119,47 @@ def test_timeout(sg):
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)
+
+
+# ------------------------------------------------------------------ the cp.async kernel's narrow tile
+
+@pytest.mark.parametrize("M,N,K,pad_a,pad_b", [(512, 512, 512, 1, 1), (257, 130, 1000, 1, 3), (1000, 200, 777, 3, 1),
+                                               (129, 65, 2000, 1, 1), (768, 640, 3000, 2, 2),
+                                               (512, 256, 1024, 4, 1),   # A 16-byte copies, B 4-byte
+                                               (512, 256, 1024, 1, 4),   # A 4-byte, B 16-byte
+                                               (300, 190, 999, 4, 2)])   # A 16-byte, B 4-byte, ragged
+def test_cp_matches_oracle(sg, M, N, K, pad_a, pad_b):
+    # rows of A and B padded so that at least one operand is not TMA-addressable
+    narrow_plan(sg, M, N, K, aligned=False)
+    A, B = gen.operands(M, N, K, seed=630 + M % 89)
+    lda = ld4(K) + 4 if pad_a == 4 else K + pad_a      # pad 4: rows 16-byte aligned
+    ldb = ld4(N) + 4 if pad_b == 4 else N + pad_b
+    C = run_sgemm(sg, A, B, lda=lda, ldb=ldb, ldc=N + 1)
+    check_full(C, A, B)
+
+
+def test_cp_unaligned_base(sg):
+    M, N, K = 384, 320, 1500
+    narrow_plan(sg, M, N, K, aligned=False)
+    A, B = gen.operands(M, N, K, seed=640)
+    check_full(run_sgemm(sg, A, B, a_off=1, b_off=2, c_off=3), A, B)
+
+
+def test_cp_wide_grid_sampled(sg):
+    M, N, K = 2048, 1024, 2048
+    narrow_plan(sg, M, N, K, aligned=False)
+    A, B = gen.operands(M, N, K, seed=641)
+    C = run_sgemm(sg, A, B, lda=K + 1, ldb=N + 1)
+    rows = [0, 1, 127, 128, 1024, M - 129, M - 2, M - 1] + list(np.random.default_rng(7).integers(0, M, 12))
+    check_rows(C, A, B, rows)
+
+
+def test_cp_integers_exact_and_repeatable(sg):
+    import torch
+    M, N, K = 384, 320, 1537
+    narrow_plan(sg, M, N, K, aligned=False)
+    A, B = gen.operands(M, N, K, seed=642, integer_copy=True)
+    c1 = run_sgemm(sg, A, B)
+    c2 = run_sgemm(sg, A, B)
+    check_full(c1, A, B, exact=True)
+    assert np.array_equal(c1, c2)
