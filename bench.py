@@ -213,13 +213,21 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- ncu traffic
 
+def code_only(text):
+    """C++ source without its comments and with runs of whitespace collapsed,
+    so that a digest follows the code a capture ran and not its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest(sources=None, tile=None):
-    """Digest of the kernel sources and, if named, the one line of TILES that
-    defines the tile configuration (so other configurations may change)."""
+    """Digest of the kernel sources' code and, if named, the one line of TILES
+    that defines the tile configuration (so other configurations may change)."""
     h = hashlib.sha256()
     for rel in sources or KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            h.update(code_only(f.read()).encode())
     if tile:
         with open(os.path.join(ROOT, TILES)) as f:
             lines = [l.strip() for l in f if l.strip().startswith(f"using {tile} =")]

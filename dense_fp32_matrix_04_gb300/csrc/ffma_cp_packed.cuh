@@ -4,13 +4,14 @@
 // FMAs, epilogue and cluster split, fed by cp.async copies that every thread
 // issues instead of TMA boxes.
 //
-//  * Copies: per k-step, the 128 x 32 slab of A and the 32 x 128 slab of B
-//    move by cp.async into the same shared-memory layout the TMA writes (A in
-//    128-byte rows with the 128-byte swizzle, chunk c of row r at c ^ (r % 8);
-//    B dense), so the arithmetic is the TMA kernel's own (tile_fma).  A warp
-//    copies one row of 32 consecutive k of A, or 32 consecutive columns of a
-//    row of B, with 4-byte copies (coalesced 128-byte requests); when an
-//    operand's rows are 16-byte aligned it uses 16-byte copies instead.
+//  * Copies: per k-step, the 128 x 32 slab of A and the 32 x BN slab of B
+//    (BN = 128, or 64 for the narrow tile) move by cp.async into the same
+//    shared-memory layout the TMA writes (A in 128-byte rows with the 128-byte
+//    swizzle, chunk c of row r at c ^ (r % 8); B dense), so the arithmetic is
+//    the TMA kernel's own (tile_fma).  A warp copies one row of 32 consecutive
+//    k of A, or 32 consecutive columns of a row of B, with 4-byte copies
+//    (coalesced 128-byte requests); when an operand's rows are 16-byte aligned
+//    it uses 16-byte copies instead.
 //  * Masking: slots outside A or B are zero-filled by the copy itself (source
 //    size 0, no global read) -- the pages' masked tile loads ("SGEMM: Shared
 //    Memory Tiling Visualizer", the tiled kernel listing).  Most copies need

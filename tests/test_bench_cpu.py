@@ -55,6 +55,9 @@ def test_recorded_traffic_follows_the_kernel_sources():
     for name, sources, tile in bench.TRAFFIC_PROFILES.values():
         assert os.path.exists(os.path.join(bench.ROOT, "profiles", name))
         assert len(bench.kernel_source_digest(sources, tile)) == 16
+    # comments do not enter the digest; code does
+    assert bench.code_only("int a; // x\n/* y\n z */ int  b;") == bench.code_only("int a;\nint b; // other")
+    assert bench.code_only("int a;") != bench.code_only("int b;")
     # the digest names one tile configuration: another one's line does not enter it
     d_main = bench.kernel_source_digest(bench.KERNEL_SOURCES, "TmaMainTile")
     assert d_main != bench.kernel_source_digest(bench.KERNEL_SOURCES, "TmaNarrowTile")
