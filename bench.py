@@ -57,8 +57,8 @@ TILES = "dense_fp32_matrix_04_gb300/csrc/tiles.cuh"
 # capture covers, the tile configuration in TILES it ran)
 TRAFFIC_PROFILES = {
     "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES, "TmaMainTile"),
-    "ragged_3001x4999x2047": ("ffma_cp_ragged_3001x4999x2047.md",
-                              ["dense_fp32_matrix_04_gb300/csrc/ffma_cp_packed.cuh"] + KERNEL_SOURCES, "TmaMainTile"),
+    "ragged_3001x4999x2047": ("ffma_phased_ragged_3001x4999x2047.md",
+                              ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_phased.cuh"] + KERNEL_SOURCES, "TmaMainTile"),
     "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES, "TmaSmallKTile"),
     "square_1024": ("ffma_narrow_square_1024.md", KERNEL_SOURCES, "TmaNarrowTile"),
 }
@@ -358,9 +358,19 @@ def kernel_name(sg, M, N, K):
             name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                      "added through distributed shared memory)")
         return name
-    name = ("sgemm_ffma_cp_kernel (128x128x32 tile fed by cp.async, 3 stages, 8x16 per thread as fma.rn.f32x2 "
-            "column pairs, 2 CTAs/SM)")
-    tiles, full, cs, _ = sg.sgemm_f32_plan(M, N, K, aligned=False) if K > 0 else (0, 0, 1, 128)
+    tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K, aligned=False) if K > 0 else (0, 0, 1, 128)
+    if M >= 4 and K >= 4:
+        # rows only 4-byte aligned: each operand read by TMA through four phase maps
+        if tn == 64:
+            return ("sgemm_ffma_tma_phased_kernel (128x64x32 narrow tile, A and B each read by TMA through four "
+                    "phase maps and realigned in shared memory, 2 stages, 8x8 per thread as fma.rn.f32x2 column "
+                    f"pairs, 4 CTAs/SM); all {tiles} tiles split over {cs}-CTA clusters (k-steps divided, partial "
+                    "sums added through distributed shared memory)")
+        name = ("sgemm_ffma_tma_phased_kernel (128x128x32 tile, A and B each read by TMA through four phase maps "
+                "and realigned in shared memory, 3 stages, 8x16 per thread as fma.rn.f32x2 column pairs, 2 CTAs/SM)")
+    else:
+        name = ("sgemm_ffma_cp_kernel (128x128x32 tile fed by cp.async, 3 stages, 8x16 per thread as fma.rn.f32x2 "
+                "column pairs, 2 CTAs/SM)")
     if cs > 1:
         name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                  "added through distributed shared memory)")

@@ -12,6 +12,7 @@
 
 #include "../../include/sgemm.h"
 #include "ffma_cp_packed.cuh"
+#include "ffma_tma_phased.cuh"
 #include "ffma_tma_sgemm.cuh"
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
@@ -35,6 +36,8 @@ using TmaTile = sgemm::TmaMainTile;
 using TmaSmallK = sgemm::TmaSmallKTile;
 using TmaNarrow = sgemm::TmaNarrowTile;
 using TmaNarrowCp = sgemm::TmaNarrowCpTile;
+using TmaPhased = sgemm::PhasedTile<sgemm::TmaMainTile>;
+using PhasedNarrow = sgemm::PhasedTile<sgemm::TmaNarrowTile>;
 using X3Tile = sgemm::Tf32x3MainTile;
 
 constexpr int kMaxDevices = 64;
@@ -45,12 +48,15 @@ constexpr int kMaxSplits = 64;
 // size forced on the cluster split of the main tile (0 = the automatic plan,
 // 1 = never split, 2 .. 8 = split the tiles beyond whole multiples of the SM
 // count with that cluster size); bit 8: put every tile in the cluster-split
-// launch; bit 9: no programmatic overlap; bit 10: never use the narrow tile.
+// launch; bit 9: no programmatic overlap; bit 10: never use the narrow tile;
+// bit 11: read 16-byte aligned operands through the phase maps as well (the
+// main tile of the phased kernel instead of the TMA kernel).
 constexpr int kDebugForceCpAsync = 2;
 constexpr int kDebugClusterShift = 4;
 constexpr int kDebugClusterAll = 256;
 constexpr int kDebugNoOverlap = 512;  // launch the cluster-split grid without programmatic overlap
 constexpr int kDebugNoNarrow = 1024;
+constexpr int kDebugForcePhased = 2048;
 std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
@@ -110,6 +116,32 @@ bool encode_2d(CUtensorMap *map, const float *ptr, int rows, int cols, int ld, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The four phase maps of a rows x cols operand (leading dimension ld, rows
+// >= 4, base 4-byte aligned): phase s holds rows s, s + 4, ..., 4 ld floats
+// apart; it starts at the 16-byte boundary d_s floats below row s, is
+// cols + d_s wide (zero past the operand's last column and last row) and is
+// read in boxes of box_rows x (box_cols + 4).  Returns d_0 .. d_3, two bits
+// each, or -1 when a map cannot be encoded.
+int encode_phases(CUtensorMap (&maps)[4], const float *ptr, int rows, int cols, int ld, int box_rows, int box_cols) {
+    auto fn = encode_fn();
+    if (!fn || rows < 4) return -1;
+    int shifts = 0;
+    for (int s = 0; s < 4; ++s) {
+        const uintptr_t row = reinterpret_cast<uintptr_t>(ptr) + (uintptr_t)s * (uintptr_t)ld * sizeof(float);
+        const int d = (int)((row >> 2) & 3);
+        const cuuint64_t dims[2] = {(cuuint64_t)cols + (cuuint64_t)d, (cuuint64_t)((rows - s + 3) / 4)};
+        const cuuint64_t strides[1] = {(cuuint64_t)4 * (cuuint64_t)ld * sizeof(float)};
+        const cuuint32_t box[2] = {(cuuint32_t)box_cols + 4, (cuuint32_t)box_rows};
+        const cuuint32_t elem[2] = {1, 1};
+        if (fn(&maps[s], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, reinterpret_cast<void *>(row - 4 * (uintptr_t)d), dims,
+               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return -1;
+        shifts |= d << (2 * s);
+    }
+    return shifts;
+}
+
 // Raise a kernel's dynamic shared-memory limit once (per device: `done` is the
 // caller's flag for this kernel and device).
 template <class Kernel>
@@ -140,7 +172,14 @@ struct Problem {
 // The TMA kernel needs 16-byte aligned bases and row strides and K >= 1.
 bool use_tma(const Problem &p) {
     return p.K > 0 && aligned16(p.A) && p.lda % 4 == 0 && aligned16(p.B) && p.ldb % 4 == 0 &&
-           !(g_debug_flags.load() & kDebugForceCpAsync);
+           !(g_debug_flags.load() & (kDebugForceCpAsync | kDebugForcePhased));
+}
+
+// Operands the TMA kernel cannot address (rows only 4-byte aligned) go through
+// four phase maps each, which need at least four rows of A and of B.
+bool use_phased(const Problem &p) {
+    const int dbg = g_debug_flags.load();
+    return p.M >= 4 && p.K >= 4 && !(dbg & kDebugForceCpAsync) && ((dbg & kDebugForcePhased) || !use_tma(p));
 }
 
 int k_tiles(const Problem &p) { return (p.K + TmaTile::BK - 1) / TmaTile::BK; }
@@ -162,6 +201,17 @@ bool tma_attr(int dev) {
     static std::atomic<int> done[kMaxDevices];
     return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC, ROLE>, T::SMEM_BYTES);
 }
+
+template <class T, bool VC, int ROLE>
+bool phased_attr(int dev) {
+    static std::atomic<int> done[kMaxDevices];
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_phased_kernel<T, VC, ROLE>, T::SMEM_BYTES);
+}
+
+template <class T>
+struct IsPhased : std::false_type {};
+template <class T>
+struct IsPhased<sgemm::PhasedTile<T>> : std::true_type {};
 
 // The cluster-split launch configuration: `clusters` clusters of cs CTAs and,
 // after a plain grid of the same product, programmatic overlap with that grid.
@@ -185,8 +235,8 @@ cudaLaunchConfig_t split_config(int64_t clusters, int cs, bool overlap, cudaStre
 }
 
 // Whether clusters of `cs` CTAs of the cluster-split kernel can be resident on
-// this device at all; queried once per device and size on the TMA form (the
-// cp.async form has the same block size, shared memory and CTAs per SM).
+// this device at all; queried once per device and size on the kernel of T
+// (the TMA, cp.async-fed or phased form).
 template <class T, bool VA, bool VB, int ROLE>
 bool cp_packed_attr(int dev);
 
@@ -199,6 +249,7 @@ bool cluster_fits(int dev, int cs) {
     if (k == 0) {
         bool smem_ok;
         if constexpr (CP) smem_ok = cp_packed_attr<T, false, false, sgemm::kRoleSplit>(dev);
+        else if constexpr (IsPhased<T>::value) smem_ok = phased_attr<T, true, sgemm::kRoleSplit>(dev);
         else smem_ok = tma_attr<T, true, sgemm::kRoleSplit>(dev);
         if (!smem_ok) return false;
         cudaLaunchAttribute attr[2];
@@ -207,6 +258,9 @@ bool cluster_fits(int dev, int cs) {
         cudaError_t e;
         if constexpr (CP)
             e = cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_cp_kernel<T, false, false, sgemm::kRoleSplit>,
+                                               &cfg);
+        else if constexpr (IsPhased<T>::value)
+            e = cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_tma_phased_kernel<T, true, sgemm::kRoleSplit>,
                                                &cfg);
         else
             e = cudaOccupancyMaxActiveClusters(&n, sgemm::sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit>, &cfg);
@@ -265,9 +319,10 @@ double narrow_sm_time(const NarrowModel &m, int64_t L, double w) {
     return (double)L * w / m.steps + m.round * (double)((L + m.per_sm - 1) / m.per_sm);
 }
 
-// Which narrow tile a product may take: none, the TMA kernel's, or the
-// cp.async kernel's.
-enum class Narrow { kNone, kTma, kCp };
+// Which narrow tile a product may take: none, the TMA kernel's, the cp.async
+// kernel's, or the phased TMA kernel's (run, like the TMA kernel's, at four
+// CTAs per SM, and planned with its model).
+enum class Narrow { kNone, kTma, kCp, kPhased };
 
 // The cluster split fills SMs that a grid would leave idle.  With P SMs, the
 // `rem` tiles beyond whole multiples of P (all of them when there are fewer
@@ -277,7 +332,7 @@ enum class Narrow { kNone, kTma, kCp };
 // fewer main tiles than SMs, the narrow tile of the product's path (`narrow`)
 // in clusters of 2, 4 or 8 (the c with the lowest estimate, ties to the
 // larger c) is taken instead when its estimate is lower still.
-SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow) {
+SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow, bool phased = false) {
     using T = TmaTile;
     SplitPlan plan;
     plan.tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
@@ -304,14 +359,15 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow)
         if (narrow != Narrow::kNone && !(dbg & kDebugNoNarrow) && plan.tiles < P) {
             static_assert(TmaNarrow::BM == TmaNarrowCp::BM && TmaNarrow::BN == TmaNarrowCp::BN, "one narrow tile shape");
             using TN = TmaNarrow;
-            const NarrowModel &m = narrow == Narrow::kTma ? kNarrowTma : kNarrowCp;
+            const NarrowModel &m = narrow == Narrow::kCp ? kNarrowCp : kNarrowTma;
             const int64_t ntiles = (int64_t)((M + TN::BM - 1) / TN::BM) * ((N + TN::BN - 1) / TN::BN);
             int ncs = 0;
             double nbest = 0.0;
             for (int c = 2; c <= 8 && kt >= 4 * c; c *= 2) {
                 const double t = narrow_sm_time(m, (ntiles * c + P - 1) / P, (double)((kt + c - 1) / c));
-                const bool fits = narrow == Narrow::kTma ? cluster_fits<TmaNarrow>(info.dev, c)
-                                                          : cluster_fits<TmaNarrowCp, true>(info.dev, c);
+                const bool fits = narrow == Narrow::kTma      ? cluster_fits<TmaNarrow>(info.dev, c)
+                                  : narrow == Narrow::kPhased ? cluster_fits<PhasedNarrow>(info.dev, c)
+                                                              : cluster_fits<TmaNarrowCp, true>(info.dev, c);
                 if ((ncs == 0 || t <= nbest) && fits) nbest = t, ncs = c;
             }
             if (ncs > 0 && nbest < best) {
@@ -324,7 +380,7 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow)
         }
     }
     if (cs < 2 || cs > 8 || full == plan.tiles) return plan;
-    if (!cluster_fits<T>(info.dev, cs)) return plan;
+    if (!(phased ? cluster_fits<TmaPhased>(info.dev, cs) : cluster_fits<T>(info.dev, cs))) return plan;
     plan.full = full;
     plan.cs = cs;
     return plan;
@@ -389,6 +445,59 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
     }
 }
 
+// Launch the phased TMA kernel (operands whose rows are only 4-byte aligned)
+// over grouped tiles [tile_base, tile_base + tiles), with the same roles as
+// launch_tma.
+template <class T>
+int launch_phased(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
+                  int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
+    static_assert(IsPhased<T>::value && T::CSPLIT_OK, "a tile read through phase maps");
+    alignas(64) sgemm::PhasedMaps maps;
+    const int da = encode_phases(maps.a, p.A, p.M, p.K, p.lda, T::A_PHASE_ROWS, T::BK);
+    const int db = encode_phases(maps.b, p.B, p.K, p.N, p.ldb, T::B_PHASE_ROWS, T::BN);
+    if (da < 0 || db < 0) return SGEMM_ERR_LAUNCH;
+    const unsigned long long wait = g_wait_limit_ns.load();
+    const int dbg = g_debug_flags.load();
+    using sgemm::sgemm_ffma_tma_phased_kernel;
+    // the narrow tile only ever runs as clusters
+    constexpr bool kClustersOnly = std::is_same_v<T, PhasedNarrow>;
+    if constexpr (kClustersOnly) {
+        if (cs <= 1) return SGEMM_ERR_LAUNCH;
+    } else if (cs <= 1) {
+        const dim3 grid((unsigned)tiles, (unsigned)splits);
+        if (primary) {
+            if (!(vc ? phased_attr<T, true, sgemm::kRolePrimary>(info.dev)
+                     : phased_attr<T, false, sgemm::kRolePrimary>(info.dev)))
+                return SGEMM_ERR_LAUNCH;
+            auto kernel = vc ? sgemm_ffma_tma_phased_kernel<T, true, sgemm::kRolePrimary>
+                             : sgemm_ffma_tma_phased_kernel<T, false, sgemm::kRolePrimary>;
+            kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(maps, (uint32_t)da, (uint32_t)db, p.M, p.N, p.K, alpha,
+                                                                beta, p.C, p.ldc, partials, ldp, (int)tile_base,
+                                                                info.err_word, wait, dbg);
+        } else {
+            if (!(vc ? phased_attr<T, true, sgemm::kRolePlain>(info.dev)
+                     : phased_attr<T, false, sgemm::kRolePlain>(info.dev)))
+                return SGEMM_ERR_LAUNCH;
+            auto kernel = vc ? sgemm_ffma_tma_phased_kernel<T, true, sgemm::kRolePlain>
+                             : sgemm_ffma_tma_phased_kernel<T, false, sgemm::kRolePlain>;
+            kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(maps, (uint32_t)da, (uint32_t)db, p.M, p.N, p.K, alpha,
+                                                                beta, p.C, p.ldc, partials, ldp, (int)tile_base,
+                                                                info.err_word, wait, dbg);
+        }
+        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
+    if (!(vc ? phased_attr<T, true, sgemm::kRoleSplit>(info.dev) : phased_attr<T, false, sgemm::kRoleSplit>(info.dev)))
+        return SGEMM_ERR_LAUNCH;
+    auto kernel = vc ? sgemm_ffma_tma_phased_kernel<T, true, sgemm::kRoleSplit>
+                     : sgemm_ffma_tma_phased_kernel<T, false, sgemm::kRoleSplit>;
+    const bool overlap = tile_base > 0 && !(dbg & kDebugNoOverlap);
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = split_config<T>(tiles, cs, overlap, stream, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, maps, (uint32_t)da, (uint32_t)db, p.M, p.N, p.K, alpha, beta,
+                                             p.C, p.ldc, (float *)nullptr, 0, (int)tile_base, info.err_word, wait, dbg);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 template <class T, bool VA, bool VB, int ROLE>
 bool cp_packed_attr(int dev) {
     static std::atomic<int> done[kMaxDevices];
@@ -440,7 +549,8 @@ int launch_cp(const Problem &p, float alpha, float beta, bool vc, int splits, fl
 }
 
 // Launch the product: on the TMA kernels when the operands allow it (the
-// small-K tile for K <= 64), otherwise on the cp.async-fed kernel.  splits > 1
+// small-K tile for K <= 64), on the phased TMA kernel when their rows are only
+// 4-byte aligned (M, K >= 4), otherwise on the cp.async-fed kernel.  splits > 1
 // writes partial sums to `partials` (splits slabs of M x ldp) instead of C;
 // splits == 1 follows the cluster-split plan.
 int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
@@ -449,7 +559,8 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     // partial slabs hold the raw products; alpha and beta act in the reduction
     const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
     const bool tma = use_tma(p);
-    if (!tma && !cp_fits(p)) {
+    const bool phased = !tma && use_phased(p);
+    if (!tma && !phased && !cp_fits(p)) {
         // rows of A more than 2 GiB apart and not 16-byte aligned: the register-
         // tiled kernel of the pages' ladder, which indexes in 64 bits (C = A B;
         // the entry points that get here pass alpha = 1, beta = 0, one split)
@@ -465,20 +576,26 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     }
     // grouped tiles [base, base + n) as a (n x s) grid, or n clusters of cs CTAs
     auto launch = [&](int64_t base, int64_t n, int s, int cs, bool primary) {
-        return tma ? launch_tma<TmaTile>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream, info)
-                   : launch_cp<TmaTile>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream, info);
+        return tma      ? launch_tma<TmaTile>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream, info)
+               : phased ? launch_phased<TmaPhased>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream,
+                                                   info)
+                        : launch_cp<TmaTile>(p, alpha, beta, vc, s, partials, ldp, base, n, cs, primary, stream, info);
     };
     if (splits > 1) {
         const int64_t tiles = (int64_t)((p.M + TmaTile::BM - 1) / TmaTile::BM) * ((p.N + TmaTile::BN - 1) / TmaTile::BN);
         return launch(0, tiles, splits, 1, false);
     }
-    const Narrow narrow = tma ? Narrow::kTma : (cp_narrow_fits(p) ? Narrow::kCp : Narrow::kNone);
-    const SplitPlan plan = split_plan(p.M, p.N, p.K, info, narrow);
+    const Narrow narrow = tma ? Narrow::kTma
+                          : phased ? Narrow::kPhased
+                                   : (cp_narrow_fits(p) ? Narrow::kCp : Narrow::kNone);
+    const SplitPlan plan = split_plan(p.M, p.N, p.K, info, narrow, phased);
     if (plan.narrow)
-        return tma ? launch_tma<TmaNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false, stream,
-                                           info)
-                   : launch_cp<TmaNarrowCp>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false,
-                                            stream, info);
+        return tma      ? launch_tma<TmaNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false,
+                                                stream, info)
+               : phased ? launch_phased<PhasedNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs,
+                                                      false, stream, info)
+                        : launch_cp<TmaNarrowCp>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false,
+                                                 stream, info);
     if (plan.full > 0) {
         const int st = launch(0, plan.full, 1, 1, plan.cs > 1);
         if (st != SGEMM_OK || plan.full == plan.tiles) return st;
@@ -697,14 +814,17 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
     if ((int64_t)M * N == 0) return SGEMM_OK;
     DeviceInfo info;
     if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
-    const bool cp = !tma_operands || (g_debug_flags.load() & kDebugForceCpAsync) != 0;
+    const int dbg = g_debug_flags.load();
+    const bool cp = !tma_operands || (dbg & (kDebugForceCpAsync | kDebugForcePhased)) != 0;
+    const bool phased = cp && M >= 4 && K >= 4 && !(dbg & kDebugForceCpAsync);
     if (K <= 2 * TmaSmallK::BK && K > 0 && !cp) {
         *tiles = *full_tiles =
             (long long)((M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((N + TmaSmallK::BN - 1) / TmaSmallK::BN);
         *tile_n = TmaSmallK::BN;
         return SGEMM_OK;
     }
-    const SplitPlan plan = split_plan(M, N, K, info, cp ? Narrow::kCp : Narrow::kTma);
+    const SplitPlan plan =
+        split_plan(M, N, K, info, !cp ? Narrow::kTma : phased ? Narrow::kPhased : Narrow::kCp, phased);
     *tiles = plan.tiles;
     *full_tiles = plan.full;
     *cluster_size = plan.cs;
@@ -741,7 +861,7 @@ int sgemm_f32_splitk(int M, int N, int K, const float *A, int lda, const float *
     // more splits than k-steps would leave empty slabs: cap at the k-step count
     const int kt = k_tiles(p);
     if (splits > kt) splits = kt > 0 ? kt : 1;
-    if (!use_tma(p) && !cp_fits(p)) splits = 1;
+    if (!use_tma(p) && !use_phased(p) && !cp_fits(p)) splits = 1;
     if (splits > 1) {
         const size_t need = partials_bytes(M, N, splits);
         if (!workspace || !aligned16(workspace) || workspace_bytes < need) return SGEMM_ERR_INVALID_ARG;
@@ -772,7 +892,7 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const
     if ((int64_t)M * N == 0) return SGEMM_OK;
     const int kt = k_tiles(p);
     if (splits > kt) splits = kt > 0 ? kt : 1;
-    if (!use_tma(p) && !cp_fits(p)) splits = 1;
+    if (!use_tma(p) && !use_phased(p) && !cp_fits(p)) splits = 1;
     const int ldp = ld_partials(N);
     if (splits > 1 && (long long)splits * M * ldp > kNoallocScratchFloats) return SGEMM_ERR_SCRATCH_LIMIT;
     DeviceInfo info;

@@ -69,9 +69,17 @@ typedef enum {
  *     4 floats), K >= 1: 128 x 128 block tiles copied by the tensor memory
  *     accelerator (TMA) with hardware zero-fill at the edges, 8 x 16 outputs
  *     per thread accumulated with packed two-wide FP32 FMAs;
- *   - otherwise (and for K == 0): the same tiles, fragment reads and packed
- *     FMAs, fed by cp.async copies (16-byte copies for an operand whose rows
- *     are 16-byte aligned, 4-byte copies otherwise).  A last, partial row of
+ *   - otherwise, with M >= 4 and K >= 4: the same tiles and packed FMAs, each
+ *     operand read by the TMA through four tensor maps, one per residue of
+ *     the row index mod 4 (those rows are 4 * ld floats apart, a multiple of
+ *     16 bytes), in boxes 4 floats wider than the tile; each row is shifted
+ *     into place in shared memory before the FMAs.  A phase map starts at the
+ *     16-byte boundary at or below its first row, so up to 3 floats in front
+ *     of a row (the previous row's tail, or for the first row the bytes
+ *     before A or B in the same 16-byte granule) are read and never used;
+ *   - otherwise (M < 4, K < 4, or K == 0): the same tiles, fragment reads and
+ *     packed FMAs, fed by cp.async copies (16-byte copies for an operand whose
+ *     rows are 16-byte aligned, 4-byte copies otherwise).  A last, partial row of
  *     tiles reads the 128 rows of A that end at row M and stores only its
  *     own; B's right edge is a per-thread copy size; only the last, partial
  *     k-step and products with M < 128 take per-element masks.  The copy
@@ -79,17 +87,18 @@ typedef enum {
  *     >= 2^31 takes 4-byte copies, and an A whose rows are not 16-byte
  *     aligned with 4 * lda >= 2^31 is computed by the pages' register-tiled
  *     ladder kernel (64-bit indexing, much slower).
- * On both paths, when a grid would leave SMs idle (few tiles, or a last
+ * On every path, when a grid would leave SMs idle (few tiles, or a last
  * partial round of tiles over the SMs), those tiles are each shared by a
  * thread-block cluster of 2, 4 or 8 blocks that split its k-steps and add their
  * partial sums through distributed shared memory in a fixed rank order: no
  * workspace, and the same bits on every run.  With fewer 128 x 128 tiles than
- * SMs, either path may instead use narrow 128 x 64 tiles (8 x 8 outputs per
- * thread; four blocks per SM on the TMA path, three on the cp.async path, the
- * latter only when 16 * lda and 8 * ldb fit in 32 bits), all in such clusters
+ * SMs, any path may instead use narrow 128 x 64 tiles (8 x 8 outputs per
+ * thread; four blocks per SM on the TMA and phased paths, three on the
+ * cp.async path, the latter only when 16 * lda and 8 * ldb fit in 32 bits),
+ * all in such clusters
  * (sgemm_f32_plan reports the choice).
  * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
- * The TMA kernel's waits are bounded: if a copy never lands, its blocks give
+ * The TMA kernels' waits are bounded: if a copy never lands, its blocks give
  * up, write nothing, and the next sgemm_device_status() returns
  * SGEMM_ERR_TIMEOUT.
  */
@@ -109,8 +118,9 @@ int sgemm_f32(int M, int N, int K,
  * *full_tiles == *tiles).  *tile_n is 64 for TMA operands with 1 <= K <= 64
  * (never split) and for the narrow tile, which a product with fewer 128 x 128
  * tiles than SMs takes when its cost model says so (then every tile is in a
- * cluster); 128 otherwise.  For non-TMA operands the plan assumes 16 * lda
- * and 8 * ldb fit in 32 bits (otherwise the 128 x 128 plan runs).  The result
+ * cluster); 128 otherwise.  Non-TMA operands with M >= 4 and K >= 4 take the
+ * phased TMA kernel's plan; smaller ones the cp.async kernel's, which assumes
+ * 16 * lda and 8 * ldb fit in 32 bits (otherwise the 128 x 128 plan runs).  The result
  * reflects the test-only switches of sgemm_debug_set.  Launches nothing.
  * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
  * if the device cannot be queried.
@@ -361,7 +371,9 @@ int sgemm_device_status(cudaStream_t stream);
  * split the tiles beyond whole multiples of the SM count with that size);
  * bit 8: with a forced size, split every tile; bit 9: no programmatic overlap
  * of the cluster-split launch with the plain one before it; bit 10: never
- * use the narrow tile (a forced cluster size also keeps the 128 x 128 tile).
+ * use the narrow tile (a forced cluster size also keeps the 128 x 128 tile);
+ * bit 11: read 16-byte aligned operands through the phase maps too (every
+ * shift 0), so the phased kernel can be checked on any inputs.
  * wait_limit_ns:
  * the bound of each wait
  * (default 2 s).  Affects every

@@ -160,7 +160,11 @@ def test_automatic_plan(sg, M, N, K):
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms)
-    # operands the TMA cannot address: the cp.async kernel's narrow tile and model
+    # operands the TMA cannot address directly: the phased TMA kernel, whose
+    # narrow tile runs like the TMA kernel's (four CTAs per SM) and takes its model
+    assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow="tma")
+    # with every product on the cp.async-fed kernel: its narrow tile and model
+    sg.sgemm_debug_set(2)
     assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow="cp")
     sg.sgemm_debug_set(NO_NARROW)
     assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms, narrow=None)

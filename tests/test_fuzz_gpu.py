@@ -1,7 +1,7 @@
 """Seeded random cases across every product entry point: random shapes
 (including 1 and values around the 128 / 64 / 32 tile edges), leading-dimension
 padding, base offsets (which move operands off 16-byte alignment and onto the
-cp.async-fed kernel), forced launch shapes (no cluster split, clusters of 2 to
+phased TMA kernel, or the cp.async-fed one), forced launch shapes (no cluster split, clusters of 2 to
 8, every tile split), split-K counts, the 3xTF32 path and the general form with
 transposes and alpha/beta -- each compared with the FP64 oracle, element by
 element, within the stated bound; C's guard bands and row gaps must stay
@@ -71,7 +71,7 @@ def _case(sg, seed):
     ldb = b_cols + int(rng.choice([0, 0, 1, 2, 4]))
     ldc = N + int(rng.choice([0, 0, 3, 4]))
     a_off, b_off, c_off = (int(rng.choice([0, 0, 1, 2])) for _ in range(3))
-    flags = int(rng.choice([0, 0, 1 << 4, (2 << 4) | 256, (3 << 4) | 256, (4 << 4), (8 << 4) | 256, 2]))
+    flags = int(rng.choice([0, 0, 1 << 4, (2 << 4) | 256, (3 << 4) | 256, (4 << 4), (8 << 4) | 256, 2, 2048]))
     sg.sgemm_debug_set(flags)
     try:
         a_buf, pa = _device_buffer(A, max(lda, 1), a_off, torch, dev)

@@ -2,7 +2,8 @@
 (which does the per-device set-up: shared-memory limits, the cluster
 occupancy query), sgemm_f32 -- on the plain grid, the cluster split alone,
 the plain grid followed by a programmatically overlapped cluster split, the
-cp.async-fed kernel and the small-K tile -- sgemm_f32_splitk, sgemm_f32_3xtf32
+phased TMA kernel (rows only 4-byte aligned), the cp.async-fed kernel (fewer
+than four rows of A) and the small-K tile -- sgemm_f32_splitk, sgemm_f32_3xtf32
 and sgemm_gemm (both algorithms, A transposed) are captured with
 torch.cuda.graph, replayed on new inputs written into the same buffers, and
 must equal the eager results bit for bit."""
@@ -37,7 +38,8 @@ def _buffers(torch, M, N, K, aligned):
     (8192, 2048, 512, True, "plain"),            # 1024 tiles: no split
     (1024, 1024, 1024, True, "split"),           # every tile in clusters
     (2048, 2048, 2048, True, "plain+split"),     # primary grid + overlapped clusters
-    (3001, 4999, 2047, False, "cp.async"),       # unaligned: cp.async-fed, with a cluster tail
+    (3001, 4999, 2047, False, "phased"),         # unaligned: phase maps, with a cluster tail
+    (3, 2000, 1001, False, "cp.async"),          # unaligned, three rows of A: cp.async-fed
     (4096, 4096, 32, True, "small-k"),
 ])
 def test_sgemm_f32_replays_bitwise(sg, M, N, K, aligned, expect):

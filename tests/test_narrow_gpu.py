@@ -16,6 +16,7 @@ from helpers import CANARY_BITS, check_full, check_rows, run_sgemm
 pytestmark = pytest.mark.gpu
 
 NO_NARROW = 1024
+FORCE_CP = 2        # route every product to the cp.async-fed kernel (test-only)
 
 
 @pytest.fixture
@@ -122,6 +123,9 @@ def test_timeout(sg):
 
 
 # ------------------------------------------------------------------ the cp.async kernel's narrow tile
+# (operands that are not TMA-addressable take the phased TMA kernel's narrow
+# tile by default, tested in test_phased_gpu.py; a test-only switch keeps these
+# on the cp.async-fed kernel)
 
 @pytest.mark.parametrize("M,N,K,pad_a,pad_b", [(512, 512, 512, 1, 1), (257, 130, 1000, 1, 3), (1000, 200, 777, 3, 1),
                                                (129, 65, 2000, 1, 1), (768, 640, 3000, 2, 2),
@@ -130,6 +134,7 @@ def test_timeout(sg):
                                                (300, 190, 999, 4, 2)])   # A 16-byte, B 4-byte, ragged
 def test_cp_matches_oracle(sg, M, N, K, pad_a, pad_b):
     # rows of A and B padded so that at least one operand is not TMA-addressable
+    sg.sgemm_debug_set(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=630 + M % 89)
     lda = ld4(K) + 4 if pad_a == 4 else K + pad_a      # pad 4: rows 16-byte aligned
@@ -140,6 +145,7 @@ def test_cp_matches_oracle(sg, M, N, K, pad_a, pad_b):
 
 def test_cp_unaligned_base(sg):
     M, N, K = 384, 320, 1500
+    sg.sgemm_debug_set(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=640)
     check_full(run_sgemm(sg, A, B, a_off=1, b_off=2, c_off=3), A, B)
@@ -147,6 +153,7 @@ def test_cp_unaligned_base(sg):
 
 def test_cp_wide_grid_sampled(sg):
     M, N, K = 2048, 1024, 2048
+    sg.sgemm_debug_set(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=641)
     C = run_sgemm(sg, A, B, lda=K + 1, ldb=N + 1)
@@ -157,6 +164,7 @@ def test_cp_wide_grid_sampled(sg):
 def test_cp_integers_exact_and_repeatable(sg):
     import torch
     M, N, K = 384, 320, 1537
+    sg.sgemm_debug_set(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=642, integer_copy=True)
     c1 = run_sgemm(sg, A, B)

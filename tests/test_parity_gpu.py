@@ -18,12 +18,13 @@ def sg(cuda_device, lib):
     return sg
 
 
-@pytest.fixture(params=["auto", "no-cluster-split", "cp.async"])
+@pytest.fixture(params=["auto", "no-cluster-split", "cp.async", "phased"])
 def path(request, sg):
     """Run the test with the library's own kernel choice, again with the TMA
-    path's cluster split switched off, and again with every product routed to
-    the cp.async kernel (test-only switches)."""
-    flags = {"auto": 0, "no-cluster-split": 1 << 4, "cp.async": 2}[request.param]
+    path's cluster split switched off, again with every product routed to the
+    cp.async kernel, and again with aligned operands read through the phase
+    maps of the phased TMA kernel (test-only switches)."""
+    flags = {"auto": 0, "no-cluster-split": 1 << 4, "cp.async": 2, "phased": 2048}[request.param]
     sg.sgemm_debug_set(flags, 2_000_000_000)
     yield request.param
     sg.sgemm_debug_set(0, 2_000_000_000)
@@ -148,7 +149,7 @@ def test_leading_dimensions(sg, path, lda_pad, ldb_pad, ldc_pad):
 
 
 @pytest.mark.parametrize("a_off,b_off,c_off", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1), (2, 2, 2)])
-def test_unaligned_base_pointers(sg, a_off, b_off, c_off):
+def test_unaligned_base_pointers(sg, path, a_off, b_off, c_off):
     M, N, K = 130, 136, 72
     A, B = gen.operands(M, N, K, seed=9)
     check_full(run_sgemm(sg, A, B, a_off=a_off, b_off=b_off, c_off=c_off), A, B)
