@@ -272,15 +272,16 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
             sg.sgemm_f32_splitk(M, N, K, dA, K, dB, N, dC, N, splits, ws, ws_bytes, handle)
         return step, (2 if splits > 1 else f32_launches(sg, M, N, K))
     if path == "gemm":
-        # sgemm_gemm, FFMA form: unaligned operands are repacked into the workspace
+        # sgemm_gemm, FFMA form, alpha = 1, beta = 0, no transposes: unaligned
+        # operands are read in place (phase maps) unless M or K is below 4
         ws_bytes = sg.sgemm_gemm_workspace_size(0, 0, 0, M, N, K)
         ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
-        cfg["path"] = "sgemm_gemm (FFMA; operands repacked when unaligned)"
+        cfg["path"] = "sgemm_gemm (FFMA, alpha = 1, beta = 0, no transposes)"
 
         def step():
             sg.sgemm_gemm(0, 0, 0, M, N, K, 1.0, dA, K, dB, N, 0.0, dC, N, ws, ws_bytes, handle)
-        # the product runs on 16-byte aligned (repacked if need be) operands: the
-        # TMA path's one or two launches; the repacking copies are not kernels of ours
+        # the same launches as sgemm_f32 (a repacking copy, below four rows, is
+        # not a kernel of ours)
         return step, f32_launches(sg, M, N, K)
     if path in LADDER:
         cfg["path"] = path

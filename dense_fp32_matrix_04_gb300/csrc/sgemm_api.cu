@@ -1003,9 +1003,12 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
         sgemm::scale_kernel<<<blocks, 256, 0, stream>>>(M, N, beta, C, ldc);
         return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
     }
-    // the FFMA form needs its workspace only for transposed or unaligned operands
-    const bool a_copy = transa || !aligned16(A) || lda % 4 != 0;
-    const bool b_copy = transb || !aligned16(B) || ldb % 4 != 0;
+    // the FFMA form needs its workspace only for transposed operands, and for
+    // operands whose rows are not 16-byte aligned when M or K is below 4 (from
+    // four rows up the phased TMA kernel reads them where they are)
+    const bool small = M < 4 || K < 4;
+    const bool a_copy = transa || (small && (!aligned16(A) || lda % 4 != 0));
+    const bool b_copy = transb || (small && (!aligned16(B) || ldb % 4 != 0));
     const size_t need = algo == SGEMM_ALGO_3XTF32 || a_copy || b_copy
                             ? sgemm_gemm_workspace_size(algo, transa, transb, M, N, K)
                             : 0;
@@ -1027,8 +1030,9 @@ int sgemm_gemm(int algo, int transa, int transb, int M, int N, int K, float alph
         return launch_3xtf32(p, workspace, stream, info);
     }
     // FFMA: transposed operands are first copied row-major into the workspace,
-    // and operands whose base or rows are not 16-byte aligned are copied there
-    // with padded rows, so that the product runs on the TMA-fed kernel
+    // and (below four rows) operands whose base or rows are not 16-byte aligned
+    // are copied there with padded rows, so that the product runs on the
+    // TMA-fed kernel
     float *w = workspace;
     if (a_copy) {
         const int ld = (int)ld4(K);

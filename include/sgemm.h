@@ -254,16 +254,19 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K,
  *   beta == 0: C is not read (NaN in C does not propagate).
  *   alpha == 0 or K == 0: A and B are not read; C = beta * C.
  *   algo: SGEMM_ALGO_FFMA -- the FP32 FFMA kernels of sgemm_f32; an operand
- *           given transposed, or whose base or leading dimension is not
- *           16-byte aligned, is first copied row-major with padded rows into
+ *           given transposed is first copied row-major with padded rows into
  *           the workspace (one memory-bound pass), so that the product runs
- *           on the TMA-fed kernel.
+ *           on the TMA-fed kernels.  An operand whose base or leading
+ *           dimension is not 16-byte aligned is read in place through phase
+ *           maps, as by sgemm_f32; only when M or K is below 4 is it copied
+ *           into the workspace as well.
  *         SGEMM_ALGO_3XTF32 -- the tensor-core path of sgemm_f32_3xtf32; its
  *           operand split reads either orientation directly.
  *   workspace: at least sgemm_gemm_workspace_size(...) bytes, caller-owned
  *           device memory, 16-byte aligned, not overlapping A, B or C; the
- *           FFMA form reads it only for transposed or unaligned operands (and
- *           may then be given NULL otherwise).
+ *           FFMA form reads it only for transposed operands, and for
+ *           unaligned ones when M or K is below 4 (and may be given NULL
+ *           otherwise).
  * Accuracy: |C - C_exact| <= 2 (K + 2) 2^-24 (|alpha| sum_k |a||b| + |beta||c|).
  * K <= 2,097,120 (and N <= 2,097,120 when B is transposed); other errors as
  * for sgemm_f32_3xtf32.

@@ -163,13 +163,31 @@ def test_bad_arguments(sg):
         sg.sgemm_gemm(0, 1, 0, 8, 8, 8, 1.0, x, 8, y, 8, 0.0, z, 8)
 
 
+@pytest.mark.parametrize("M,N,K", [(190, 170, 150), (3, 170, 150), (190, 170, 2)])
 @pytest.mark.parametrize("a_off,lda_pad,ldb_pad", [(1, 0, 0), (0, 1, 0), (0, 0, 3), (2, 5, 1)])
-def test_unaligned_operands_are_repacked(sg, a_off, lda_pad, ldb_pad):
-    # FFMA form with unaligned A or B: the product must not change, only its kernel
-    M, N, K = 190, 170, 150
+def test_unaligned_operands(sg, M, N, K, a_off, lda_pad, ldb_pad):
+    # FFMA form with unaligned A or B: read in place through phase maps, or
+    # (M or K below 4) repacked into the workspace; the product must not
+    # change, only its kernel
     A, B, C0 = stored(M, N, K, 0, 0, seed=117)
     C = run_gemm(sg, 0, 0, 0, 1.0, A, B, 0.0, C0, lda=K + lda_pad, ldb=N + ldb_pad, a_off=a_off)
     check_general(C, 0, 0, 1.0, A, B, 0.0, C0)
+
+
+def test_unaligned_operands_need_no_workspace(sg):
+    import torch
+    M, N, K = 260, 300, 333
+    A, B, C0 = stored(M, N, K, 0, 0, seed=118)
+    dA = torch.zeros(M * (K + 1) + 1, device="cuda")
+    dB = torch.zeros(K * (N + 3), device="cuda")
+    for r in range(M):
+        dA[1 + r * (K + 1): 1 + r * (K + 1) + K] = torch.from_numpy(A[r]).cuda()
+    for r in range(K):
+        dB[r * (N + 3): r * (N + 3) + N] = torch.from_numpy(B[r]).cuda()
+    dC = torch.full((M, N), float("nan"), device="cuda")
+    sg.sgemm_gemm(0, 0, 0, M, N, K, 0.5, dA.data_ptr() + 4, K + 1, dB, N + 3, 0.0, dC, N, None, 0)
+    torch.cuda.synchronize()
+    check_general(dC.cpu().numpy(), 0, 0, 0.5, A, B, 0.0, C0)
 
 
 def test_ragged_workload_through_sgemm_gemm(sg):
