@@ -104,7 +104,10 @@ __device__ __forceinline__ void tile_fma_phased(uint64_t (&acc2)[T::TM][T::TN / 
 #pragma unroll
                 for (int j = 0; j < T::TN / 2; ++j)
 #pragma unroll
-                    for (int i = 0; i < T::TM; ++i) f32x2_fma(acc2[i][j], ad[i], b2[j]);
+                    for (int ii = 0; ii < T::TM; ++ii) {  // rows down and up in turn, as tile_fma
+                        const int i = (T::MIN_BLOCKS < 4 && (j & 1)) ? T::TM - 1 - ii : ii;
+                        f32x2_fma(acc2[i][j], ad[i], b2[j]);
+                    }
             } else {
 #pragma unroll
                 for (int i = 0; i < T::TM; ++i) {

@@ -133,7 +133,11 @@ __device__ __forceinline__ void tile_fma(float (&acc)[T::PACKED ? 1 : T::TM][T::
                     b2[2 * q + 1] = v.y;
                 }
                 if (T::ORDER == 1) {
-                    // column-pair outer: one B pair reused down the TM rows
+                    // column-pair outer: one B pair reused down the TM rows; with
+                    // more than 128 registers a thread, the rows are walked down and
+                    // up in turn so that the last A value of one column pair is the
+                    // first of the next (measured 1-2 % faster than restarting at
+                    // row 0; at 128 registers it spills)
                     uint64_t ad[T::TM];
 #pragma unroll
                     for (int i = 0; i < T::TM; ++i)
@@ -141,7 +145,10 @@ __device__ __forceinline__ void tile_fma(float (&acc)[T::PACKED ? 1 : T::TM][T::
 #pragma unroll
                     for (int j = 0; j < T::TN / 2; ++j)
 #pragma unroll
-                        for (int i = 0; i < T::TM; ++i) f32x2_fma(acc2[i][j], ad[i], b2[j]);
+                        for (int ii = 0; ii < T::TM; ++ii) {
+                            const int i = (T::MIN_BLOCKS < 4 && (j & 1)) ? T::TM - 1 - ii : ii;
+                            f32x2_fma(acc2[i][j], ad[i], b2[j]);
+                        }
                 } else {
                     // row outer: one duplicated A value reused across the row of pairs
 #pragma unroll
