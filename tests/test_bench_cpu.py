@@ -48,8 +48,11 @@ def test_recorded_traffic_follows_the_kernel_sources():
     # each committed ncu summary carries the digest of the kernel headers it was taken on
     t = bench.recorded_traffic()
     assert t is None or t > 805_306_368       # at least the algorithmic bytes when present
+    # the ragged product's 125.5 MB fit in L2: ncu (which empties the caches
+    # before a captured launch) sees A and B come from DRAM, but part of C may
+    # still sit in L2 when the launch ends, so only the operand reads bound it
     r = bench.recorded_traffic("ragged_3001x4999x2047")
-    assert r is None or r > 4 * (3001 * 2047 + 2047 * 4999 + 3001 * 4999)
+    assert r is None or r > 4 * (3001 * 2047 + 2047 * 4999)
     assert bench.recorded_traffic("tiny_6x6x9") is None
     assert len(bench.kernel_source_digest()) == 16
     for name, sources, tile in bench.TRAFFIC_PROFILES.values():
