@@ -83,3 +83,36 @@ def test_bad_level(sg):
     x = torch.zeros(16, device="cuda")
     with pytest.raises(sg.SgemmError):
         sg.sgemm_f32_ladder(9, 2, 2, 2, x, 2, x.data_ptr() + 16, 2, x.data_ptr() + 32, 2)
+
+
+# ------------------------------------------------- the product kernels against the naive kernel
+# Every product kernel of sgemm_f32 adds its k-terms to each output in order,
+# k = 0, 1, ..., K - 1, one round-to-nearest FMA per term starting from zero --
+# packed two to an instruction, but each half an ordinary FP32 FMA -- exactly as
+# the pages' naive kernel does with one scalar fmaf per term.  So when no k-split
+# divides the sum (a plain grid of 128 x 128 tiles, test-only cluster size 1),
+# the results must agree bit for bit.
+
+NO_SPLIT = 1 << 4
+FORCE_CP = 2
+FORCE_PHASED = 2048
+
+
+@pytest.mark.parametrize("path,flags,pad", [("tma", NO_SPLIT, 4), ("small-k tma", 0, 4),
+                                            ("phased", NO_SPLIT, 1), ("phased, aligned", NO_SPLIT | FORCE_PHASED, 4),
+                                            ("cp.async", NO_SPLIT | FORCE_CP, 1)])
+@pytest.mark.parametrize("M,N,K", [(300, 260, 777), (129, 520, 64), (640, 384, 1000)])
+def test_product_kernels_equal_the_naive_kernel_bitwise(sg, path, flags, pad, M, N, K):
+    if path == "small-k tma" and K > 64:
+        pytest.skip("the small-K tile takes K <= 64")
+    A, B = gen.operands(M, N, K, seed=90 + M % 13)
+    lda = (K + 3) // 4 * 4 if pad == 4 else K + pad
+    ldb = (N + 3) // 4 * 4 if pad == 4 else N + pad
+    naive = run_ladder(sg, 0, A, B, lda=lda, ldb=ldb)
+    from helpers import run_sgemm
+    sg.sgemm_debug_set(flags)
+    try:
+        C = run_sgemm(sg, A, B, lda=lda, ldb=ldb)
+    finally:
+        sg.sgemm_debug_set(0)
+    assert np.array_equal(C, naive), f"{path}: {np.count_nonzero(C != naive)} outputs differ from the naive kernel"
