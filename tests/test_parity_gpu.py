@@ -76,6 +76,8 @@ def test_ragged_3001x4999x2047(sg):
     rr = np.repeat(np.arange(0, M, 7), cols.size)
     cc = np.tile(cols, np.arange(0, M, 7).size)
     check_entries(C, A, B, rr, cc)
+    # and every element (the oracle's 6.1e10 FP64 multiply-adds take a few seconds)
+    check_full(C, A, B)
 
 
 def test_square_8192_sampled(sg):
