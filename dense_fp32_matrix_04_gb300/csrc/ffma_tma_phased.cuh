@@ -16,7 +16,8 @@
 //  * After a stage lands, every warp shifts its share of the rows with d_s > 0
 //    left by d_s floats in place (read the row, __syncwarp, write it back),
 //    before the CTA barrier that precedes the stage's FMAs.  The per-thread
-//    FMAs and the epilogue are the TMA kernel's.
+//    FMAs, their order and the epilogue's arithmetic are the TMA kernel's;
+//    only the shared-memory addresses and the row map differ.
 //  * The stage keeps the boxes as they land, phase by phase: A's rows in
 //    phase-major order (tile row 4 q + s at shared row s * BM/4 + q, 144-byte
 //    pitch: the 36-float box row) and B's k-rows likewise (k = 4 q + s at
@@ -25,6 +26,9 @@
 //    different 16-byte bank groups (the pages' padding, "Memory hierarchy --
 //    visual walkthrough", Step 6), and the epilogue maps shared row rho back
 //    to tile row 4 (rho mod BM/4) + rho / (BM/4).
+//  * Measured on GB300 against per-thread cp.async copies of the same tile:
+//    3001 x 4999 x 2047 (lda 2047, ldb 4999) 51.9 -> 57.2 TFLOP/s, 8192^3
+//    with lda = ldb = 8193 59.9 -> 63.5, results bit-identical.
 // The reuse scheme is that of the aligned kernel: block tiles staged in shared
 // memory ("SGEMM: Shared Memory Tiling Visualizer"), per-thread register outer
 // products ("SGEMM: 2D Register Tiling Visualizer"), and masking done by the
