@@ -162,3 +162,26 @@ def test_narrow_tile_integers_exact_and_repeatable(sg):
     c2 = run_sgemm(sg, A, B, lda=K + 2, ldb=N + 1, b_off=3)
     check_full(c1, A, B, exact=True)
     assert np.array_equal(c1, c2)
+
+
+def test_rows_more_than_2_gib_apart(sg):
+    # lda = 2^29 + 1 floats: the phase maps' row pitch (16 lda bytes, 8 GiB) and
+    # the offsets of A's rows exceed 32 bits; the product is still exact
+    import torch
+    from oracle import ref_gemm
+    M, N, K = 4, 40, 9              # one row per phase of A: 6.4 GB of buffer
+    lda, ldb = (1 << 29) + 1, N + 1
+    A, B = gen.operands(M, N, K, seed=480, integer_copy=True)
+    dA = torch.zeros((M - 1) * lda + K, device="cuda")
+    dB = torch.zeros((K - 1) * ldb + N, device="cuda")
+    for r in range(M):
+        dA[r * lda: r * lda + K] = torch.from_numpy(A[r]).cuda()
+    for r in range(K):
+        dB[r * ldb: r * ldb + N] = torch.from_numpy(B[r]).cuda()
+    assert sg.sgemm_f32_plan(M, N, K, aligned=False)[3] == 128
+    C = torch.full((M, N), float("nan"), device="cuda")
+    sg.sgemm_f32(M, N, K, dA, lda, dB, ldb, C, N)
+    torch.cuda.synchronize()
+    C64, _ = ref_gemm.gemm_f64(A, B)
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), C64)
+    del dA, dB
