@@ -46,8 +46,9 @@
 
 namespace sgemm {
 
-// The four phase maps of each operand (A: M x K, B: K x N, row-major) and
-// their shifts, two bits per phase (bits 2 s .. 2 s + 1 hold d_s).
+// The four phase maps of each operand (A: M x K, B: K x N, row-major).  The
+// kernel takes their shifts separately, two bits per phase (bits 2 s and
+// 2 s + 1 hold d_s).
 struct PhasedMaps {
     CUtensorMap a[4];
     CUtensorMap b[4];
