@@ -163,15 +163,16 @@ def test_bad_arguments(sg):
         sg.sgemm_gemm(0, 1, 0, 8, 8, 8, 1.0, x, 8, y, 8, 0.0, z, 8)
 
 
+@pytest.mark.parametrize("alpha,beta", [(1.0, 0.0), (-0.75, 1.5)])
 @pytest.mark.parametrize("M,N,K", [(190, 170, 150), (3, 170, 150), (190, 170, 2)])
 @pytest.mark.parametrize("a_off,lda_pad,ldb_pad", [(1, 0, 0), (0, 1, 0), (0, 0, 3), (2, 5, 1)])
-def test_unaligned_operands(sg, M, N, K, a_off, lda_pad, ldb_pad):
+def test_unaligned_operands(sg, M, N, K, a_off, lda_pad, ldb_pad, alpha, beta):
     # FFMA form with unaligned A or B: read in place through phase maps, or
     # (M or K below 4) repacked into the workspace; the product must not
     # change, only its kernel
     A, B, C0 = stored(M, N, K, 0, 0, seed=117)
-    C = run_gemm(sg, 0, 0, 0, 1.0, A, B, 0.0, C0, lda=K + lda_pad, ldb=N + ldb_pad, a_off=a_off)
-    check_general(C, 0, 0, 1.0, A, B, 0.0, C0)
+    C = run_gemm(sg, 0, 0, 0, alpha, A, B, beta, C0, lda=K + lda_pad, ldb=N + ldb_pad, a_off=a_off)
+    check_general(C, 0, 0, alpha, A, B, beta, C0)
 
 
 def test_unaligned_operands_need_no_workspace(sg):
