@@ -354,7 +354,7 @@ def kernel_name(sg, M, N, K):
                     f"fma.rn.f32x2 column pairs, 4 CTAs/SM); all {tiles} tiles split over {cs}-CTA clusters "
                     "(k-steps divided, partial sums added through distributed shared memory)")
         name = ("sgemm_ffma_tma_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as fma.rn.f32x2 "
-                "column pairs, 2 CTAs/SM)")
+                "column pairs with the rows walked down and up in turn, 2 CTAs/SM)")
         if cs > 1:
             name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                      "added through distributed shared memory)")
@@ -368,10 +368,15 @@ def kernel_name(sg, M, N, K):
                     f"pairs, 4 CTAs/SM); all {tiles} tiles split over {cs}-CTA clusters (k-steps divided, partial "
                     "sums added through distributed shared memory)")
         name = ("sgemm_ffma_tma_phased_kernel (128x128x32 tile, A and B each read by TMA through four phase maps "
-                "and realigned in shared memory, 3 stages, 8x16 per thread as fma.rn.f32x2 column pairs, 2 CTAs/SM)")
+                "and realigned in shared memory, 3 stages, 8x16 per thread as fma.rn.f32x2 column pairs with the "
+                "rows walked down and up in turn, 2 CTAs/SM)")
+    elif tn == 64:
+        return ("sgemm_ffma_cp_kernel (128x64x32 narrow tile fed by cp.async, 3 stages, 8x8 per thread as "
+                f"fma.rn.f32x2 column pairs, 3 CTAs/SM); all {tiles} tiles split over {cs}-CTA clusters (k-steps "
+                "divided, partial sums added through distributed shared memory)")
     else:
         name = ("sgemm_ffma_cp_kernel (128x128x32 tile fed by cp.async, 3 stages, 8x16 per thread as fma.rn.f32x2 "
-                "column pairs, 2 CTAs/SM)")
+                "column pairs with the rows walked down and up in turn, 2 CTAs/SM)")
     if cs > 1:
         name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                  "added through distributed shared memory)")
