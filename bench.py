@@ -59,7 +59,7 @@ TRAFFIC_PROFILES = {
     "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES, "TmaMainTile"),
     "ragged_3001x4999x2047": ("ffma_phased_ragged_3001x4999x2047.md",
                               ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_phased.cuh"] + KERNEL_SOURCES, "TmaMainTile"),
-    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES, "TmaSmallKTile"),
+    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES, "TmaSmallK1Tile"),
     "square_1024": ("ffma_narrow_square_1024.md", KERNEL_SOURCES, "TmaNarrowTile"),
 }
 
@@ -347,7 +347,7 @@ def kernel_name(sg, M, N, K):
     if K > 0 and K % 4 == 0 and N % 4 == 0:
         if K <= 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed small-K tile, 1 stage, 8x8 per thread as "
-                    "fma.rn.f32x2 column pairs, 4 CTAs/SM)")
+                    f"fma.rn.f32x2 column pairs, k-groups unrolled by {4 if K <= 32 else 8}, 4 CTAs/SM)")
         tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
         if tn == 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed narrow tile, 2 stages, 8x8 per thread as "

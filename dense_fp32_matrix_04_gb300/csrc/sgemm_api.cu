@@ -34,6 +34,7 @@ namespace {
 
 using TmaTile = sgemm::TmaMainTile;
 using TmaSmallK = sgemm::TmaSmallKTile;
+using TmaSmallK1 = sgemm::TmaSmallK1Tile;
 using TmaNarrow = sgemm::TmaNarrowTile;
 using TmaNarrowCp = sgemm::TmaNarrowCpTile;
 using TmaPhased = sgemm::PhasedTile<sgemm::TmaMainTile>;
@@ -445,6 +446,24 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
     }
 }
 
+// One k-step (K <= 32) with C's rows 16-byte aligned: the small-K tile unrolled
+// by four, as a plain grid of `tiles` tiles (its scalar-store form would spill,
+// so it is built only with 16-byte C stores).
+int launch_smallk1(const Problem &p, float alpha, float beta, int64_t tiles, cudaStream_t stream,
+                   const DeviceInfo &info) {
+    using T = TmaSmallK1;
+    static_assert(T::BM == TmaSmallK::BM && T::BN == TmaSmallK::BN, "one small-K tile shape");
+    alignas(64) CUtensorMap ta, tb;
+    if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return SGEMM_ERR_LAUNCH;
+    if (!tma_attr<T, true, sgemm::kRolePlain>(info.dev)) return SGEMM_ERR_LAUNCH;
+    sgemm::sgemm_ffma_tma_kernel<T, true, sgemm::kRolePlain><<<(unsigned)tiles, T::THREADS, T::SMEM_BYTES, stream>>>(
+        ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc, nullptr, 0, 0, info.err_word, g_wait_limit_ns.load(),
+        g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Launch the phased TMA kernel (operands whose rows are only 4-byte aligned)
 // over grouped tiles [tile_base, tile_base + tiles), with the same roles as
 // launch_tma.
@@ -572,6 +591,7 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     if (tma && splits == 1 && p.K <= 2 * TmaSmallK::BK) {
         const int64_t tiles =
             (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
+        if (p.K <= TmaSmallK1::BK && vc) return launch_smallk1(p, alpha, beta, tiles, stream, info);
         return launch_tma<TmaSmallK>(p, alpha, beta, vc, 1, partials, ldp, 0, tiles, 1, false, stream, info);
     }
     // grouped tiles [base, base + n) as a (n x s) grid, or n clusters of cs CTAs
