@@ -322,7 +322,14 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                 (void)mbar_wait_bounded(bars + 8 * (t % T::STAGES), (t / T::STAGES) & 1, wait_limit_ns);
         }
         __syncthreads();
-        if constexpr (!CSPLIT) return;
+        if constexpr (!CSPLIT) {
+            if (gridDim.y <= 1) return;
+            // a split-K slab is filled with NaN instead (no stale partials reach C)
+#pragma unroll
+            for (int i = 0; i < T::TM; ++i)
+#pragma unroll
+                for (int j = 0; j < T::TN / 2; ++j) acc2[i][j] = 0x7fc000007fc00000ull;
+        }
     }
 
     if constexpr (CSPLIT) {

@@ -290,6 +290,21 @@ __device__ __forceinline__ void store_tile(const float (&acc)[T::PACKED ? 1 : T:
     }
 }
 
+// Quiet NaN in every accumulator: what a CTA that gave up writes to its
+// split-K slab.
+template <class T>
+__device__ __forceinline__ void poison_tile(float (&acc)[T::PACKED ? 1 : T::TM][T::PACKED ? 1 : T::TN],
+                                            uint64_t (&acc2)[T::PACKED ? T::TM : 1][T::PACKED ? T::TN / 2 : 1]) {
+#pragma unroll
+    for (int i = 0; i < (T::PACKED ? 1 : T::TM); ++i)
+#pragma unroll
+        for (int j = 0; j < (T::PACKED ? 1 : T::TN); ++j) acc[i][j] = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int i = 0; i < (T::PACKED ? T::TM : 1); ++i)
+#pragma unroll
+        for (int j = 0; j < (T::PACKED ? T::TN / 2 : 1); ++j) acc2[i][j] = 0x7fc000007fc00000ull;
+}
+
 // What a launch of the kernel does: a plain grid of tiles; the same, as the
 // first of a plain + cluster-split pair (it lets the second grid start early);
 // or the cluster-split grid.
@@ -415,7 +430,12 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         }
         __syncthreads();
         // a cluster-split CTA still takes part in both cluster barriers below
-        if constexpr (!CSPLIT) return;
+        if constexpr (!CSPLIT) {
+            if (gridDim.y <= 1) return;
+            // a split-K slab is filled with NaN instead, so that the reduction
+            // cannot add stale partial sums into C
+            poison_tile<T>(acc, acc2);
+        }
     }
 
     if constexpr (CSPLIT) {

@@ -920,8 +920,10 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const
     if (splits == 1) return launch_product(p, 1, nullptr, 0, stream, info);
     float *scratch = nullptr;
     if (noalloc_scratch(&scratch) != SGEMM_OK) return SGEMM_ERR_DEVICE;
-    // every (split, row < M, column < N) partial is written by the product
-    // kernel before the reduction reads it, so nothing needs clearing
+    // every (split, row < M, column < N) partial that the reduction adds into C
+    // is written by the product kernels first (as NaN by a block that gave up
+    // on a wait); the padding columns it also reads are discarded, so nothing
+    // needs clearing
     st = launch_product(p, splits, scratch, ldp, stream, info);
     if (st != SGEMM_OK) return st;
     return launch_reduce(p, splits, scratch, ldp, stream, info);

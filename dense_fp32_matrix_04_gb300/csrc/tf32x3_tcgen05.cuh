@@ -273,8 +273,18 @@ __global__ void __launch_bounds__(T::THREADS, 1)
                 }
             }
         }
-    } else if (tid == 0) {
-        atomicCAS(err_word, 0, 1);
+    } else {
+        if (tid == 0) atomicCAS(err_word, 0, 1);
+        if (gridDim.y > 1) {
+            // a partial slab is filled with NaN, so that the reduction cannot add
+            // stale partial sums into C
+            const int row = m0 + 32 * warp + lane;
+            if (row < M) {
+                const float q[4] = {__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                    __int_as_float(0x7fc00000), __int_as_float(0x7fc00000)};
+                for (int c = 0; c < T::BN; c += 4) store_quad<VEC_C>(C + (int64_t)row * ldc, n0 + c, N, q, 1.f, 0.f);
+            }
+        }
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -147,8 +147,8 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
  * SGEMM_ERR_INVALID_ARG for a bad split count or a missing, misaligned or
  * short workspace; SGEMM_ERR_ALIAS if the workspace overlaps an operand.  If
  * a product kernel gives up on a bounded wait (SGEMM_ERR_TIMEOUT from
- * sgemm_device_status), the reduction still runs and C holds unspecified
- * values.
+ * sgemm_device_status), it fills its partial tile with NaN instead, and the
+ * reduction, which still runs, makes the elements of C in that tile NaN.
  */
 int sgemm_f32_splitk(int M, int N, int K,
                      const float *A, int lda,
@@ -196,8 +196,8 @@ int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
  * partial tiles of a divided product.  Any alignment of A, B and C is
  * accepted.  K <= 2,097,120.  K == 0 writes zeros and needs no workspace.
  * Errors as for sgemm_f32_splitk; the copy waits are bounded and report
- * through sgemm_device_status (after a timeout of a divided product C holds
- * unspecified values).
+ * through sgemm_device_status (after a timeout of a divided product, the
+ * elements of C in the tiles that gave up are NaN).
  */
 int sgemm_f32_3xtf32(int M, int N, int K,
                      const float *A, int lda,
@@ -231,11 +231,17 @@ size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K);
  * current); make that first call before any stream capture.
  *
  * Every call on a device shares the one array, and the array keeps the last
- * call's partials.  Nothing in it needs to start at zero: each call writes
- * every partial it later reads.  Calls whose kernels overlap on the GPU (on
- * different streams, or from different threads) race on the array and give
- * wrong results: order them on one stream or with events.  Arguments, results
- * and the other error codes are as for sgemm_f32_splitk.
+ * call's partials.  Nothing in it needs to start at zero: the product kernels
+ * of a call write every partial sum that its reduction adds into C (rows < M,
+ * columns < N of each split's slab) before the reduction runs.  The reduction
+ * also reads the padding columns of a slab (N up to the next multiple of 4),
+ * which may hold an earlier call's values; it discards them.  A product kernel
+ * that gives up on a bounded wait fills its partial tile with NaN, so an
+ * earlier call's partials never reach C (those elements of C are NaN).  Calls
+ * whose kernels overlap on the GPU (on different streams, or from different
+ * threads) race on the array and give wrong results: order them on one stream
+ * or with events.  Arguments, results and the other error codes are as for
+ * sgemm_f32_splitk.
  */
 int sgemm_f32_splitk_noalloc(int M, int N, int K,
                              const float *A, int lda,

@@ -64,20 +64,22 @@ def test_bitwise_equal_to_the_main_tile(sg, K):
     assert torch.equal(c1, c2)
 
 
-def test_alpha_beta(sg):
+@pytest.mark.parametrize("K", [40, 32, 20])   # two k-steps; one k-step (the tile unrolled by four); one, ragged
+def test_alpha_beta(sg, K):
     from oracle import ref_gemm, tolerance
     from test_gemm_general_gpu import run_gemm
-    A = gen.matrix(312, gen.STREAM_A, 700, 40)
-    B = gen.matrix(312, gen.STREAM_B, 40, 900)
+    A = gen.matrix(312, gen.STREAM_A, 700, K)
+    B = gen.matrix(312, gen.STREAM_B, K, 900)
     C0 = gen.matrix(313, gen.STREAM_A, 700, 900)
     C = run_gemm(sg, 0, 0, 0, 1.75, A, B, -0.5, C0)
     C64, S, T = ref_gemm.gemm_general_f64(False, False, 1.75, A, B, -0.5, C0)
-    assert tolerance.max_error_ratio_general(C, C64, S, T, 40, 1.75) <= 1.0
+    assert tolerance.max_error_ratio_general(C, C64, S, T, K, 1.75) <= 1.0
 
 
-def test_timeout_with_many_ctas(sg):
+@pytest.mark.parametrize("K", [64, 32])   # the small-K tile, and its one-k-step form unrolled by four
+def test_timeout_with_many_ctas(sg, K):
     import torch
-    M, N, K = 2048, 4096, 64
+    M, N = 2048, 4096
     A, B = gen.operands(M, N, K, seed=314)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()

@@ -68,3 +68,56 @@ def test_noalloc_refuses_requests_beyond_its_fixed_array(cuda_device, lib):
     assert st == sg.SGEMM_ERR_SCRATCH_LIMIT
     torch.cuda.synchronize()
     assert bool((dC == 7.0).all())
+
+
+def _noalloc_against_oracle(lib, M, N, K, splits, seed):
+    import torch
+
+    import dense_fp32_matrix_04_gb300 as sg
+    A, B = gen.operands(M, N, K, seed=seed)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.full((M, N), float("nan"), device="cuda")
+    st = lib.sgemm_f32_splitk_noalloc(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N, splits,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert st == sg.SGEMM_OK, sg.status_string(st)
+    torch.cuda.synchronize()
+    C64, S = ref_gemm.gemm_f64(A, B)
+    assert tolerance.max_error_ratio(dC.cpu().numpy(), C64, S, K) <= 1.0
+
+
+def test_noalloc_request_that_exactly_fills_the_array(cuda_device, lib):
+    # 8 splits x 1024 rows x 1024 columns = 8,388,608 floats, the whole array
+    _noalloc_against_oracle(lib, 1024, 1024, 256, 8, 62)
+
+
+def test_noalloc_request_that_fits_only_after_the_split_count_is_lowered(cuda_device, lib):
+    # K = 64 has two 32-deep k-steps, so 64 splits become 2: 2 x 2048 x 2048 floats
+    # fill the array exactly, while 64 x 2048 x 2048 would not fit
+    _noalloc_against_oracle(lib, 2048, 2048, 64, 64, 63)
+
+
+def test_noalloc_timeout_leaves_no_stale_partials_in_c(cuda_device, lib):
+    # a first call leaves valid partial sums in the shared array; a second call
+    # whose copies never land (test-only switch) must not add them into C: the
+    # blocks that give up fill their partial tiles with NaN
+    import torch
+
+    import dense_fp32_matrix_04_gb300 as sg
+    M, N, K, splits = 512, 512, 512, 4
+    _noalloc_against_oracle(lib, M, N, K, splits, 64)
+    sg.sgemm_device_status()
+    A, B = gen.operands(M, N, K, seed=65)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), device="cuda")
+    sg.sgemm_debug_set(1, 50_000_000)
+    try:
+        st = lib.sgemm_f32_splitk_noalloc(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N, splits,
+                                          torch.cuda.current_stream().cuda_stream)
+        assert st == sg.SGEMM_OK
+        assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
+    finally:
+        sg.sgemm_debug_set(0, 2_000_000_000)
+    assert bool(torch.isnan(dC).all())
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    # and the next call is correct again
+    _noalloc_against_oracle(lib, M, N, K, splits, 66)
