@@ -46,6 +46,9 @@ import gen  # noqa: E402
 
 METRIC = "SGEMM TFLOP/s (2MNK/t) and % of FP32 roofline at M=N=K=8192"
 DEFAULT_WORKLOAD = "square_8192"
+# the other workloads, each measured in the line's "configs" block
+CONFIG_WORKLOADS = ["tiny_6x6x9", "square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32"]
+FLUSH_BYTES = 256 * 2 ** 20   # twice L2: written between steps of workloads that fit in L2
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 FP32_LANES_PER_SM = 128
@@ -71,7 +74,7 @@ def log(*a):
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=150)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS))
@@ -86,6 +89,12 @@ def parse_args():
                    help="skip the torch.matmul (cuBLAS SGEMM) context timing")
     p.add_argument("--no-variants", action="store_true",
                    help="skip the extra 3xTF32 measurement reported beside the headline")
+    p.add_argument("--configs", default=",".join(CONFIG_WORKLOADS),
+                   help="comma-separated workloads measured beside the headline in the 'configs' block "
+                        "('' for none)")
+    p.add_argument("--min-seconds", type=float, default=2.0,
+                   help="wall time of each config's timed region, and of the sustained load under which the "
+                        "headline's clocks are sampled")
     return p.parse_args()
 
 
@@ -320,6 +329,28 @@ def f32_launches(sg, M, N, K):
     return 1
 
 
+TF32_PEAK_NOTE = ("DERIVED, not measured: dense TF32 tensor peak = {tsrc}; the tensor-core kernel alone "
+                  "reads at or above it, so this peak is low and frac overstates the kernel's use of the "
+                  "tensor pipe")
+TF32_PROFILES = {"square_8192": "tf32x3_tcgen05_square_8192.md"}
+TF32_SOURCES = ["dense_fp32_matrix_04_gb300/csrc/tf32x3_tcgen05.cuh", "dense_fp32_matrix_04_gb300/csrc/ptx.cuh",
+                "dense_fp32_matrix_04_gb300/csrc/tile_map.cuh"]
+
+
+def recorded_tensor_pipe(workload):
+    """The tensor-pipe busy fraction ncu measured for the 3xTF32 kernel on this
+    workload (from its committed summary), or None."""
+    try:
+        text = open(os.path.join(ROOT, "profiles", TF32_PROFILES[workload])).read()
+    except (KeyError, OSError):
+        return None
+    m = re.search(r"tensor_pipe_active_pct:\s*([0-9.]+)", text)
+    d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_source_digest(TF32_SOURCES):
+        return None
+    return float(m.group(1)) / 100
+
+
 def tf32_peak_tflops():
     """Dense TF32 tensor peak: the measured bf16 burst peak x the nominal TF32/bf16 ratio (1.1/2.25)."""
     try:
@@ -381,6 +412,128 @@ def kernel_name(sg, M, N, K):
         name += (f"; tiles {full}..{tiles - 1} split over {cs}-CTA clusters (k-steps divided, partial sums "
                  "added through distributed shared memory)")
     return name
+
+
+def alu_peak_tflops(sms, mhz=MAX_SM_MHZ):
+    return sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+
+
+def config_roofline(M, N, K, ms, sms, hbm_gbs, hbm_src, clocks):
+    """Roofline of one product: achieved 2MNK/t against min(FP32 ALU peak,
+    intensity x HBM bandwidth), the intensity over the algorithmic bytes
+    4(MK + KN + MN)."""
+    flop = 2.0 * M * N * K
+    alg_bytes = 4 * (M * K + K * N + M * N)
+    p_alu = alu_peak_tflops(sms)
+    p_hbm = flop / alg_bytes * hbm_gbs * 1e9 / 1e12
+    achieved = flop / (ms / 1e3) / 1e12
+    r = {"bound": "alu" if p_alu <= p_hbm else "hbm", "achieved": achieved, "unit": "TFLOP/s",
+         "peak": min(p_alu, p_hbm), "frac": achieved / min(p_alu, p_hbm),
+         "peak_basis": (f"min({sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {MAX_SM_MHZ:.0f} MHz = "
+                        f"{p_alu:.2f}, {flop / alg_bytes:.1f} FLOP/B x {hbm_gbs:.0f} GB/s ({hbm_src}) = "
+                        f"{p_hbm:.2f}) TFLOP/s"),
+         "algorithmic_bytes": alg_bytes, "alu_floor_ms": flop / (p_alu * 1e12) * 1e3,
+         "hbm_floor_ms": alg_bytes / (hbm_gbs * 1e9) * 1e3}
+    if clocks.get("sm_mhz") and r["bound"] == "alu":
+        r["frac_at_sampled_clock"] = achieved / alu_peak_tflops(sms, clocks["sm_mhz"])
+    return r
+
+
+def timed_steps(step, stream, dev, flush_buf, min_s, max_steps=200000):
+    """Run ``step`` for about ``min_s`` seconds of wall time; return (steps, device ms per step).
+    With ``flush_buf`` every step is timed between its own events, after a
+    write of the buffer (twice L2) outside them; otherwise the steps run back
+    to back between two events."""
+    import torch
+    # probe the wall cost of one step (with its flush) to size the region
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(5):
+        if flush_buf is not None:
+            flush_buf.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    per = (time.perf_counter() - t0) / 5
+    n = int(min(max_steps, max(5, -(-min_s // max(per, 1e-6)))))
+    if flush_buf is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return n, e0.elapsed_time(e1) / n
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        flush_buf.fill_(1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return n, sum(a.elapsed_time(b) for a, b in evs) / n
+
+
+def measure_config(sg, name, dev, stream, sms, props, min_s, flush_buf):
+    """One entry of the "configs" block: the workload through sgemm_f32 with
+    its inputs resident in HBM (device time over a timed region of about
+    ``min_s`` seconds, clocks sampled during it), its roofline, a check of
+    sampled rows against the oracle, and the same product end to end through
+    sgemm_f32_host with host buffers."""
+    import numpy as np
+    import torch
+
+    from oracle import ref_gemm, tolerance
+    M, N, K, dist_name, seed, cfg = workload_config(name)
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist_name)
+    dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    dC = torch.empty((M, N), dtype=torch.float32, device=dev)
+    handle = stream.cuda_stream
+    step, launches = make_step(sg, "ffma", M, N, K, dA, dB, dC, handle, cfg, dev)
+    alg_bytes = 4 * (M * K + K * N + M * N)
+    flush = flush_buf if alg_bytes <= 2 * L2_BYTES and name != "tiny_6x6x9" else None
+    for _ in range(3):
+        step()
+    sampler = ClockSampler(str(getattr(props, "uuid", "")))
+    sampler.start()
+    steps, ms = timed_steps(step, stream, dev, flush, min_s)
+    clocks = sampler.stop()
+    hbm_gbs, hbm_src = measured_hbm_gbs()
+    entry = {"workload": cfg["workload"], "M": M, "N": N, "K": K, "path": "sgemm_f32",
+             "kernel": kernel_name(sg, M, N, K), "steps": steps, "ms_per_step": ms,
+             "value": 2.0 * M * N * K / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+             "l2": ("each step between its own events after a 256 MB buffer write (outside them)" if flush is not None
+                    else "back-to-back calls (launch-latency bound; 576 bytes of operands)" if name == "tiny_6x6x9"
+                    else "inputs larger than L2; no flush"),
+             "roofline": config_roofline(M, N, K, ms, sms, hbm_gbs, hbm_src, clocks),
+             "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+             "gpu_launches": steps * launches}
+    entry["roofline"]["traffic"] = recorded_traffic(name)
+    if name == "tiny_6x6x9":
+        entry["us_per_call"] = ms * 1e3
+        entry["roofline"]["note"] = "launch-latency bound: 648 FLOP per call"
+    # the oracle on sampled rows of the timed output
+    rows = sorted({0, M // 2, M - 1} | ({127, 128} if M > 128 else set()))
+    C64, S = ref_gemm.gemm_f64(np.ascontiguousarray(A[rows]), B)
+    entry["check"] = {"rows": rows, "max_error_over_bound": tolerance.max_error_ratio(dC[rows].cpu().numpy(), C64,
+                                                                                       S, K)}
+    # end to end: host buffers in, host buffer out, every copy inside the timed region
+    hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    panels = 1 if M * N < 2 ** 20 else 8
+    ws_bytes = sg.sgemm_f32_host_workspace_size(M, N, K, panels)
+    ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def e2e_step():
+        sg.sgemm_f32_host(M, N, K, hA, K, hB, N, hC, N, panels, ws, ws_bytes, handle, s_in, s_out)
+    for _ in range(2):
+        e2e_step()
+    e_steps, e_ms = timed_steps(e2e_step, stream, dev, None, min(min_s, 1.0), max_steps=20000)
+    entry["e2e"] = {"value": 2.0 * M * N * K / (e_ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+                    "steps": e_steps, "h2d_bytes_per_step": int(hA.numel() * 4 + hB.numel() * 4),
+                    "d2h_bytes_per_step": int(hC.numel() * 4),
+                    "call": f"sgemm_f32_host, {panels} row panel(s) requested, copies overlapped with the product"}
+    return entry
 
 
 def max_over_ranks(value, world, device):
@@ -479,10 +632,22 @@ def run_ours(args):
     flush = alg_bytes <= 2 * L2_BYTES
     flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush else None
 
+    torch.cuda.synchronize(dev)
+    tw = time.perf_counter()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    per_step_s = (time.perf_counter() - tw) / max(1, args.warmup)
+    # the clock record spans a sustained load of about --min-seconds: the same
+    # product, untimed, right before the timed steps, with the sampler running
+    # through both (the timed region alone may be too short for 200 ms samples)
+    soak = int(max(0, -(-(args.min_seconds - per_step_s * args.steps) // max(per_step_s, 1e-6))))
+    soak = min(soak, 100000)
     sampler.start()
+    for i in range(soak):
+        step()
+        if i % 64 == 63:
+            torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -508,6 +673,8 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
+    clocks["window"] = (f"{soak} untimed steps of the same product right before the {args.steps} timed steps, "
+                        "sampled every 200 ms through both")
     t_ms = max_over_ranks(t_ms, world, dev)
 
     flop = 2.0 * M * N * K
@@ -536,7 +703,8 @@ def run_ours(args):
     if args.path == "3xtf32":
         tpk, tsrc = tf32_peak_tflops()
         roofline = {"bound": "tensor", "achieved": 3 * flop / per_launch_s / 1e12, "peak": tpk, "unit": "TFLOP/s",
-                    "peak_basis": f"dense TF32 tensor peak, {tsrc}", "traffic": None,
+                    "peak_basis": TF32_PEAK_NOTE.format(tsrc=tsrc), "traffic": None,
+                    "tensor_pipe_active_ncu": recorded_tensor_pipe(args.workload),
                     "algorithmic_bytes": alg_bytes,
                     "kernel": "split kernels + sgemm_3xtf32_kernel (tcgen05 kind::tf32, 128x256 tiles, 3 MMAs "
                               "per k-slice); achieved counts the 3 TF32 products per FP32 product over the whole "
@@ -569,8 +737,11 @@ def run_ours(args):
                          "unit": "TFLOP/s", "ms_per_step": vt / vsteps, "steps": vsteps, "gpu_launches": vsteps * vl,
                          "roofline": {"bound": "tensor", "achieved": 3 * vval / world, "peak": tpk,
                                       "unit": "TFLOP/s", "frac": 3 * vval / world / tpk,
-                                      "peak_basis": f"dense TF32, {tsrc}",
-                                      "note": "3 TF32 products per FP32 product; split passes included"}})
+                                      "peak_basis": TF32_PEAK_NOTE.format(tsrc=tsrc),
+                                      "tensor_pipe_active_ncu": recorded_tensor_pipe(args.workload),
+                                      "note": "3 TF32 products per FP32 product over the whole step (operand "
+                                              "splitting included); the hardware's own tensor-pipe counter "
+                                              "(tensor_pipe_active_ncu) is the measured fraction"}})
 
     # context, not this library: cuBLAS SGEMM through torch.matmul with TF32 off,
     # on the same inputs, timed the same way (outside the timed region)
@@ -636,15 +807,29 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(A, B, args.cpu_seconds)
 
+    # every other workload, each through sgemm_f32 over its own timed region
+    configs = {}
+    names = [c for c in args.configs.split(",") if c] if args.path == "ffma" and world == 1 else []
+    if names:
+        del hA, hB, hC, h_ws
+        flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        for name in names:
+            t0 = time.time()
+            configs[name] = measure_config(sg, name, dev, stream, sms, props, args.min_seconds, flush_buf)
+            log(f"[bench] config {name}: {configs[name]['value']:.2f} TFLOP/s "
+                f"({configs[name]['roofline']['frac']:.3f} of roofline) in {time.time() - t0:.1f} s")
+        del flush_buf
+
     if rank == 0:
         line = {
             "metric": metric_name(args.workload), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": cfg, "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples",
-                                                                "power_w_max")},
+                                                                "power_w_max", "window")},
             "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * launches_per_step, "cpu_baseline": cpu,
             "check": check, "device": props.name, "sms": sms, "variants": variants, "context": context,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -323,12 +323,14 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         }
         __syncthreads();
         if constexpr (!CSPLIT) {
-            if (gridDim.y <= 1) return;
+            if (!T::SLABS_OK || gridDim.y <= 1) return;
             // a split-K slab is filled with NaN instead (no stale partials reach C)
+            if constexpr (T::SLABS_OK) {
 #pragma unroll
-            for (int i = 0; i < T::TM; ++i)
+                for (int i = 0; i < T::TM; ++i)
 #pragma unroll
-                for (int j = 0; j < T::TN / 2; ++j) acc2[i][j] = 0x7fc000007fc00000ull;
+                    for (int j = 0; j < T::TN / 2; ++j) acc2[i][j] = 0x7fc000007fc00000ull;
+            }
         }
     }
 

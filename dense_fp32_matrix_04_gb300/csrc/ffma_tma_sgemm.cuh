@@ -82,6 +82,10 @@ struct TmaTile {
     static constexpr int SMEM_BYTES = STAGES * STAGE + 1024 /* alignment slack */ + 8 * STAGES /* barriers */;
     // the cluster split parks a CTA's packed partial sums (and a flag word) in its stage buffers
     static constexpr bool CSPLIT_OK = PACKED && TM * TN * THREADS * 4 + 16 <= STAGES * STAGE;
+    // launched with split-K rows (gridDim.y > 1, partial slabs): only the tiles
+    // of at most two CTAs per SM (the 128 x 128 tile); the others keep their
+    // register budget free of the slab-only code
+    static constexpr bool SLABS_OK = MIN_BLOCKS <= 2;
     static_assert(TN % 4 == 0, "columns come in 4-wide quads");
     static_assert(BM <= 256 && BN <= 256, "a TMA box spans at most 256 elements per dimension");
     static_assert(BK * 4 == 128, "A rows must be exactly one 128-byte swizzle span");
@@ -431,10 +435,10 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
         __syncthreads();
         // a cluster-split CTA still takes part in both cluster barriers below
         if constexpr (!CSPLIT) {
-            if (gridDim.y <= 1) return;
+            if (!T::SLABS_OK || gridDim.y <= 1) return;
             // a split-K slab is filled with NaN instead, so that the reduction
             // cannot add stale partial sums into C
-            poison_tile<T>(acc, acc2);
+            if constexpr (T::SLABS_OK) poison_tile<T>(acc, acc2);
         }
     }
 

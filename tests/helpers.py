@@ -95,3 +95,42 @@ def check_entries(C, A, B, rows, cols):
     r = tolerance.max_error_ratio(C[rows, cols], c64, s, A.shape[1])
     assert r <= 1.0, f"sampled entries: error/bound {r:.3g}"
     return r
+
+
+# Operands and oracle results of the large workloads, kept for the session so
+# that the FFMA and 3xTF32 tests of one workload draw and check them once.
+_OPERANDS = {}
+_ORACLE = {}
+CACHE_ORACLE_BELOW = 2 ** 26 + 1   # outputs up to 8192 x 8192 (1 GB of FP64 results) are kept
+
+
+def workload_operands(name):
+    """(A, B) of a named workload, generated once per session."""
+    import gen
+    if name not in _OPERANDS:
+        M, N, K, dist, seed = gen.WORKLOADS[name]
+        _OPERANDS[name] = gen.operands(M, N, K, seed=seed, dist=dist)
+    return _OPERANDS[name]
+
+
+def check_full_blocked(C, A, B, key=None, block_rows=512):
+    """Compare every element of a large product with the oracle, computed in
+    blocks of rows (bounded host memory); return the max error/bound ratio over
+    all M x N outputs.  With ``key`` (and an output of at most 2^26 elements)
+    the oracle's blocks are kept for the next product of the same inputs."""
+    M, K = A.shape
+    cache = key is not None and M * B.shape[1] < CACHE_ORACLE_BELOW
+    blocks = _ORACLE.get(key) if cache else None
+    if blocks is None:
+        blocks = (( r0, *ref_gemm.gemm_f64(np.ascontiguousarray(A[r0:r0 + block_rows]), B))
+                  for r0 in range(0, M, block_rows))
+        if cache:
+            blocks = list(blocks)
+            _ORACLE[key] = blocks
+    worst = 0.0
+    for r0, C64, S in blocks:
+        r = tolerance.max_error_ratio(C[r0:r0 + C64.shape[0]], C64, S, K)
+        assert r <= 1.0, f"rows {r0}..{r0 + C64.shape[0] - 1}: error exceeds 2*K*u*sum|a||b| by {r:.3g}"
+        worst = max(worst, r)
+    print(f"every one of {M} x {B.shape[1]} outputs checked: max error/bound {worst:.3g}")
+    return worst

@@ -70,3 +70,24 @@ def test_recorded_traffic_follows_the_kernel_sources():
 def test_tf32_peak_derivation():
     peak, basis = bench.tf32_peak_tflops()
     assert 400 < peak < 1200 and "1.1/2.25" in basis
+
+
+def test_config_roofline_takes_the_lower_ceiling():
+    # 16384 x 16384 x 32: 15.9 FLOP/B x 6681.5 GB/s = 106.5 TFLOP/s is above the
+    # 152-SM FP32 peak of 80.55, so the FP32 pipes bound it
+    r = bench.config_roofline(16384, 16384, 32, 0.3, 152, 6681.5, "measured", {"sm_mhz": 2070.0})
+    assert r["bound"] == "alu" and abs(r["peak"] - 80.548) < 0.01
+    assert abs(r["achieved"] - 2 * 16384 * 16384 * 32 / 0.3e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    assert abs(r["frac_at_sampled_clock"] - r["frac"]) < 1e-12
+    # a product of intensity 1.1 FLOP/B is bound by HBM bandwidth
+    r = bench.config_roofline(6, 6, 9, 0.004, 152, 6681.5, "measured", {})
+    assert r["bound"] == "hbm" and r["peak"] < 80
+    assert r["algorithmic_bytes"] == 4 * (6 * 9 + 9 * 6 + 6 * 6)
+
+
+def test_every_bench_config_is_a_known_workload():
+    import gen
+    assert set(bench.CONFIG_WORKLOADS) <= set(gen.WORKLOADS)
+    assert bench.DEFAULT_WORKLOAD not in bench.CONFIG_WORKLOADS
+    assert set(bench.CONFIG_WORKLOADS) | {bench.DEFAULT_WORKLOAD} == set(gen.WORKLOADS)

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import gen
-from helpers import check_entries, check_full, check_rows, run_sgemm
+from helpers import check_entries, check_full, check_full_blocked, check_rows, run_sgemm, workload_operands
 from oracle import ref_gemm
 
 pytestmark = pytest.mark.gpu
@@ -64,7 +64,7 @@ def _sample(M, N, rng, n=400):
 
 def test_ragged_3001x4999x2047(sg):
     M, N, K, dist, seed = gen.WORKLOADS["ragged_3001x4999x2047"]
-    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    A, B = workload_operands("ragged_3001x4999x2047")
     C = _device_product(sg, A, B)
     assert np.isfinite(C).all()
     # first/last rows of the first and the ragged last block row, plus random rows
@@ -77,25 +77,27 @@ def test_ragged_3001x4999x2047(sg):
     cc = np.tile(cols, np.arange(0, M, 7).size)
     check_entries(C, A, B, rr, cc)
     # and every element (the oracle's 6.1e10 FP64 multiply-adds take a few seconds)
-    check_full(C, A, B)
+    check_full_blocked(C, A, B, key="ragged_3001x4999x2047")
 
 
-def test_square_8192_sampled(sg):
+def test_square_8192_full(sg):
     M, N, K, dist, seed = gen.WORKLOADS["square_8192"]
-    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    A, B = workload_operands("square_8192")
     C = _device_product(sg, A, B)
     assert np.isfinite(C).all()
+    # sampled rows and entries first (a quick first failure), then every element
     check_rows(C, A, B, [0, 1, 127, 128, 4095, 4096, 8190, 8191])
     check_entries(C, A, B, *_sample(M, N, np.random.default_rng(2), 2000))
+    check_full_blocked(C, A, B, key="square_8192")
 
 
-def test_skinny_16384x16384x32_sampled(sg):
+def test_skinny_16384x16384x32_full(sg):
     M, N, K, dist, seed = gen.WORKLOADS["skinny_16384x16384x32"]
-    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    A, B = workload_operands("skinny_16384x16384x32")
     C = _device_product(sg, A, B)
     assert np.isfinite(C).all()
     check_rows(C, A, B, [0, 127, 128, 8191, 16383] + list(np.random.default_rng(4).integers(0, M, 27)))
-    check_entries(C, A, B, *_sample(M, N, np.random.default_rng(5), 20000))
+    check_full_blocked(C, A, B, key="skinny_16384x16384x32")
 
 
 # ------------------------------------------------------------------ exactness

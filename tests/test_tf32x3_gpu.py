@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 
 import gen
-from helpers import CANARY_BITS, GUARD, WS_GUARD, _device_buffer, check_entries, check_full, check_rows
+from helpers import (CANARY_BITS, GUARD, WS_GUARD, _device_buffer, check_entries, check_full,
+                     check_full_blocked, check_rows, workload_operands)
 
 pytestmark = pytest.mark.gpu
 
@@ -100,28 +101,31 @@ def _device_x3(sg, A, B):
     return C.cpu().numpy()
 
 
-def test_ragged_3001x4999x2047(sg):
+def test_ragged_3001x4999x2047_full(sg):
     M, N, K, dist, seed = gen.WORKLOADS["ragged_3001x4999x2047"]
-    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    A, B = workload_operands("ragged_3001x4999x2047")
     C = _device_x3(sg, A, B)
     check_rows(C, A, B, [0, 1, 127, 128, 2999, 3000] + list(np.random.default_rng(3).integers(0, M, 20)))
+    check_full_blocked(C, A, B, key="ragged_3001x4999x2047")
 
 
-def test_square_8192_sampled(sg):
+def test_square_8192_full(sg):
     M, N, K, dist, seed = gen.WORKLOADS["square_8192"]
-    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    A, B = workload_operands("square_8192")
     C = _device_x3(sg, A, B)
     assert np.isfinite(C).all()
     check_rows(C, A, B, [0, 127, 128, 4095, 8191])
     rng = np.random.default_rng(6)
     check_entries(C, A, B, rng.integers(0, M, 2000), rng.integers(0, N, 2000))
+    check_full_blocked(C, A, B, key="square_8192")
 
 
-def test_skinny_sampled(sg):
+def test_skinny_full(sg):
     M, N, K, dist, seed = gen.WORKLOADS["skinny_16384x16384x32"]
-    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    A, B = workload_operands("skinny_16384x16384x32")
     C = _device_x3(sg, A, B)
     check_rows(C, A, B, [0, 16383] + list(np.random.default_rng(7).integers(0, M, 10)))
+    check_full_blocked(C, A, B, key="skinny_16384x16384x32")
 
 
 def test_timeout_path(sg):
