@@ -445,15 +445,20 @@ def timed_steps(step, stream, dev, flush_buf, min_s, max_steps=200000):
     write of the buffer (twice L2) outside them; otherwise the steps run back
     to back between two events."""
     import torch
-    # probe the wall cost of one step (with its flush) to size the region
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(5):
-        if flush_buf is not None:
-            flush_buf.fill_(1)
-        step()
-    torch.cuda.synchronize(dev)
-    per = (time.perf_counter() - t0) / 5
+
+    # probe the wall cost of one step (with its flush) to size the region: the
+    # second of two rounds, after one-time costs have settled
+    def probe(k):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(k):
+            if flush_buf is not None:
+                flush_buf.fill_(1)
+            step()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / k
+    per = probe(5)
+    per = probe(int(min(200, max(5, 0.1 / max(per, 1e-6)))))
     n = int(min(max_steps, max(5, -(-min_s // max(per, 1e-6)))))
     if flush_buf is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
