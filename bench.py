@@ -513,6 +513,26 @@ def measure_config(sg, name, dev, stream, sms, props, min_s, flush_buf):
              "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
              "gpu_launches": steps * launches}
     entry["roofline"]["traffic"] = recorded_traffic(name)
+    # products with fewer tiles than resident blocks: the stream-K entry point too
+    sk_bytes = sg.sgemm_f32_streamk_workspace_size(M, N, K)
+    if sk_bytes > 0:
+        sk_ws = torch.empty(sk_bytes // 4, dtype=torch.float32, device=dev)
+
+        def sk_step():
+            sg.sgemm_f32_streamk(M, N, K, dA, K, dB, N, dC, N, sk_ws, sk_bytes, handle)
+        for _ in range(3):
+            sk_step()
+        sampler = ClockSampler(str(getattr(props, "uuid", "")))
+        sampler.start()
+        sk_n, sk_ms = timed_steps(sk_step, stream, dev, flush, min_s)
+        sk_clocks = sampler.stop()
+        entry["variants"] = [{
+            "path": "sgemm_f32_streamk (equal runs of (tile, k-step) units per resident block; caller workspace "
+                    f"of {sk_bytes / 2 ** 20:.1f} MiB, allocated untimed)",
+            "steps": sk_n, "ms_per_step": sk_ms, "value": 2.0 * M * N * K / (sk_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "roofline": config_roofline(M, N, K, sk_ms, sms, hbm_gbs, hbm_src, sk_clocks),
+            "clocks": {k: sk_clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+            "gpu_launches": sk_n, "memsets": sk_n}]
     if name == "tiny_6x6x9":
         entry["us_per_call"] = ms * 1e3
         entry["roofline"]["note"] = "launch-latency bound: 648 FLOP per call"

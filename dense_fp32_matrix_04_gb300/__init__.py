@@ -65,6 +65,11 @@ _SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_void_p]),
     "sgemm_f32_3xtf32_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "sgemm_f32_streamk": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.c_void_p]),
+    "sgemm_f32_streamk_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "sgemm_f32_splitk_suggest": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.POINTER(ctypes.c_int)]),
     "sgemm_f32_ladder": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -180,6 +185,36 @@ def sgemm_f32_3xtf32(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: i
     st = lib.sgemm_f32_3xtf32(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
                               _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "sgemm_f32_3xtf32")
+
+
+def sgemm_f32_streamk(M: int, N: int, K: int, A, lda: int, B, ldb: int, C, ldc: int, workspace,
+                      workspace_bytes: int, stream=None) -> None:
+    """Stream-K C = A * B with a caller-owned device workspace (include/sgemm.h)."""
+    lib = load()
+    st = lib.sgemm_f32_streamk(int(M), int(N), int(K), _ptr(A), int(lda), _ptr(B), int(ldb), _ptr(C), int(ldc),
+                               _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "sgemm_f32_streamk")
+
+
+def sgemm_f32_streamk_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load().sgemm_f32_streamk_workspace_size(int(M), int(N), int(K)))
+
+
+def matmul_streamk(A, B, out=None, workspace=None, stream=None):
+    """Stream-K product of CUDA tensors; allocates the workspace with torch if none is given."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    need = sgemm_f32_streamk_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(max(need // 4, 4), dtype=torch.float32, device=A.device)
+    lda, ldb, ldc = _rows(A, "A"), _rows(B, "B"), _rows(out, "out")
+    sgemm_f32_streamk(M, N, K, A, lda, B, ldb, out, ldc, workspace, workspace.numel() * 4, stream)
+    return out
 
 
 def sgemm_f32_3xtf32_workspace_size(M: int, N: int, K: int) -> int:

@@ -14,6 +14,7 @@
 #include "ffma_cp_packed.cuh"
 #include "ffma_tma_phased.cuh"
 #include "ffma_tma_sgemm.cuh"
+#include "ffma_tma_streamk.cuh"
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
 #include "tf32x3_tcgen05.cuh"
@@ -58,6 +59,8 @@ constexpr int kDebugClusterAll = 256;
 constexpr int kDebugNoOverlap = 512;  // launch the cluster-split grid without programmatic overlap
 constexpr int kDebugNoNarrow = 1024;
 constexpr int kDebugForcePhased = 2048;
+constexpr int kDebugForceStreamK = 4096;  // sgemm_f32_streamk: stream-K whatever the tile count
+constexpr int kDebugStreamKPerSmShift = 13;  // bits 13..14: stream-K blocks per SM (0 = one)
 std::atomic<int> g_debug_flags{0};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
@@ -637,6 +640,95 @@ int launch_reduce(const Problem &p, int splits, const float *partials, int ldp, 
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
+// ---- stream-K (sgemm_f32_streamk)
+
+using StreamKTile = TmaTile;
+
+template <class T, bool VC>
+bool streamk_attr(int dev) {
+    static std::atomic<int> done[kMaxDevices];
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_streamk_kernel<T, VC>, T::SMEM_BYTES);
+}
+
+// CTAs of the stream-K kernel resident at once on this device (SMs x blocks
+// per SM), queried once per device; 0 if the query fails.
+template <class T>
+int64_t streamk_resident(const DeviceInfo &info) {
+    static std::atomic<int> per_sm[kMaxDevices];
+    int n = per_sm[info.dev].load(std::memory_order_acquire);
+    if (n == 0) {
+        if (!streamk_attr<T, true>(info.dev) || !streamk_attr<T, false>(info.dev)) return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgemm::sgemm_ffma_tma_streamk_kernel<T, true>,
+                                                          T::THREADS, T::SMEM_BYTES) != cudaSuccess ||
+            n < 1) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        per_sm[info.dev].store(n, std::memory_order_release);
+    }
+    return (int64_t)n * info.sms;
+}
+
+// How sgemm_f32_streamk runs a product: stream-K over a grid of `ctas` CTAs
+// (use == true), or sgemm_f32's own launch (no workspace).  Stream-K is taken
+// for TMA-addressable operands when sgemm_f32's plan (plain tiles, cluster
+// split, narrow tiles) would start fewer CTAs than the device has SMs -- few
+// output tiles over a long K, where at most eight CTAs can share a tile --
+// and then runs one CTA per SM.  Measured on GB300 (TFLOP/s, sgemm_f32 against
+// stream-K): 256 x 256 x 65536 22.3 / 41.0, 128 x 128 x 131072 5.6 / 17.8,
+// 384 x 384 x 16384 26.6 / 38.9; where sgemm_f32 fills the SMs stream-K was
+// not faster (1024^3 39.9 / 34.1, 2048^3 58.9 / 54, 512 x 512 x 32768 48.6 /
+// 50.4, 640 x 640 x 4096 44.1 / 37.9): two CTAs per SM pull apart (the older
+// one's warps issue first, the younger then runs alone) and each shared tile
+// costs a partial store and a fix-up.
+struct StreamKPlan {
+    bool use = false;
+    int64_t tiles = 0, ctas = 0;
+    size_t counter_bytes = 0, bytes = 0;
+};
+
+StreamKPlan streamk_plan(const Problem &p, const DeviceInfo &info) {
+    using T = StreamKTile;
+    StreamKPlan plan;
+    if (!use_tma(p) || (int64_t)p.M * p.N == 0 || p.K <= 2 * TmaSmallK::BK) return plan;
+    plan.tiles = (int64_t)((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN);
+    const int dbg = g_debug_flags.load();
+    if (!(dbg & kDebugForceStreamK)) {
+        const SplitPlan sp = split_plan(p.M, p.N, p.K, info, Narrow::kTma);
+        const int64_t ctas = sp.narrow ? sp.tiles * sp.cs : sp.full + (sp.tiles - sp.full) * sp.cs;
+        if (ctas >= info.sms) return plan;
+    }
+    int64_t resident = streamk_resident<T>(info);
+    if (resident <= 0) return plan;
+    const int forced = (dbg >> kDebugStreamKPerSmShift) & 3;
+    const int64_t want = (int64_t)(forced > 0 ? forced : 1) * info.sms;
+    if (want < resident) resident = want;
+    const int64_t units = plan.tiles * k_tiles(p);
+    plan.use = true;
+    plan.ctas = units < resident ? units : resident;
+    plan.counter_bytes = (size_t)((plan.tiles * 4 + 255) / 256 * 256);
+    plan.bytes = plan.counter_bytes + (size_t)(2 * plan.ctas) * T::BM * T::BN * 4;
+    return plan;
+}
+
+int launch_streamk(const Problem &p, const StreamKPlan &plan, void *workspace, cudaStream_t stream,
+                   const DeviceInfo &info) {
+    using T = StreamKTile;
+    alignas(64) CUtensorMap ta, tb;
+    if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return SGEMM_ERR_LAUNCH;
+    int *counters = static_cast<int *>(workspace);
+    unsigned char *slots = static_cast<unsigned char *>(workspace) + plan.counter_bytes;
+    if (cudaMemsetAsync(counters, 0, (size_t)plan.tiles * 4, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
+    const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
+    auto kernel = vc ? sgemm::sgemm_ffma_tma_streamk_kernel<T, true> : sgemm::sgemm_ffma_tma_streamk_kernel<T, false>;
+    kernel<<<(unsigned)plan.ctas, T::THREADS, T::SMEM_BYTES, stream>>>(
+        ta, tb, p.M, p.N, p.K, p.alpha, p.beta, p.C, p.ldc, counters, slots, info.err_word, g_wait_limit_ns.load(),
+        g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Byte range [lo, hi) spanned by a rows x cols matrix with leading dimension ld.
 void span(const void *ptr, int64_t rows, int64_t cols, int64_t ld, uintptr_t &lo, uintptr_t &hi) {
     lo = reinterpret_cast<uintptr_t>(ptr);
@@ -927,6 +1019,40 @@ int sgemm_f32_splitk_noalloc(int M, int N, int K, const float *A, int lda, const
     st = launch_product(p, splits, scratch, ldp, stream, info);
     if (st != SGEMM_OK) return st;
     return launch_reduce(p, splits, scratch, ldp, stream, info);
+}
+
+size_t sgemm_f32_streamk_workspace_size(int M, int N, int K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return 0;
+    // the plan depends on the operands only through use_tma: size it for
+    // 16-byte aligned operands, the only ones stream-K runs on (no pointer is
+    // dereferenced)
+    alignas(16) static const float aligned_probe[4] = {0.f, 0.f, 0.f, 0.f};
+    const Problem p{M, N, K, aligned_probe, (K + 3) / 4 * 4, aligned_probe, (N + 3) / 4 * 4, nullptr, N};
+    const StreamKPlan plan = streamk_plan(p, info);
+    return plan.use ? plan.bytes : 0;
+}
+
+int sgemm_f32_streamk(int M, int N, int K, const float *A, int lda, const float *B, int ldb, float *C, int ldc,
+                      float *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const Problem p{M, N, K, A, lda, B, ldb, C, ldc};
+    const int st = validate(p);
+    if (st != SGEMM_OK || (int64_t)M * N == 0) return st;
+    DeviceInfo info;
+    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
+    const StreamKPlan plan = streamk_plan(p, info);
+    if (!plan.use) return launch_product(p, 1, nullptr, 0, stream, info);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < plan.bytes) return SGEMM_ERR_INVALID_ARG;
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), w1 = w0 + plan.bytes;
+    uintptr_t lo, hi;
+    span(C, M, N, ldc, lo, hi);
+    if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+    span(A, M, K, lda, lo, hi);
+    if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+    span(B, K, N, ldb, lo, hi);
+    if (overlap(w0, w1, lo, hi)) return SGEMM_ERR_ALIAS;
+    return launch_streamk(p, plan, workspace, stream, info);
 }
 
 size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K) { return x3_workspace_bytes(M, N, K, device_sms()); }

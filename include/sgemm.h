@@ -169,6 +169,44 @@ size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits);
 int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
 
 /*
+ * Stream-K form of sgemm_f32 for products with few output tiles over a long
+ * K (e.g. 256 x 256 x 65536), where even thread-block clusters of eight
+ * blocks per tile would leave SMs idle -- the load imbalance "Shared Memory
+ * Tiling" ('What tiling does not fix') points at.  The product is cut into
+ * units of one 128 x 128 tile and one 32-deep k-step, and one block per SM
+ * takes an equal contiguous run of them across tile boundaries, with the
+ * tiled kernel of sgemm_f32 (TMA-fed tiles, packed FP32 FMAs).  A tile shared
+ * by several blocks is finished by whichever arrives last: it adds the
+ * partial tiles in k order (so every run gives the same bits) and stores the
+ * tile.  Each element is an FP32 sum of FP32 products within the bound
+ * stated above, and exact for small integers.
+ *   Stream-K runs when A and B are 16-byte aligned with leading dimensions
+ *   that are multiples of 4, K > 64, and sgemm_f32's own plan would start
+ *   fewer blocks than the device has SMs.  Every other product runs exactly
+ *   as sgemm_f32 does and reads no workspace.
+ *   workspace: caller-owned device memory of at least
+ *     sgemm_f32_streamk_workspace_size(M, N, K) bytes (0 when the product
+ *     does not take stream-K), 16-byte aligned, not overlapping A, B or C: one
+ *     counter per tile, which the call zeroes (a memset on `stream`) before
+ *     its kernel, and two partial tiles per block.  Its contents on entry do
+ *     not matter.  Calls that share a workspace must not overlap on the GPU.
+ * Errors as for sgemm_f32_splitk.  The copy waits are bounded; a block that
+ * gives up stops, so the tiles it shares are not stored (C keeps its old
+ * values there) and sgemm_device_status reports SGEMM_ERR_TIMEOUT.
+ */
+int sgemm_f32_streamk(int M, int N, int K,
+                      const float *A, int lda,
+                      const float *B, int ldb,
+                      float *C, int ldc,
+                      float *workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* Workspace bytes sgemm_f32_streamk needs for an M x N x K product of
+ * 16-byte aligned operands on the current device (0 when it runs as
+ * sgemm_f32). */
+size_t sgemm_f32_streamk_workspace_size(int M, int N, int K);
+
+/*
  * C = A * B in FP32 accuracy on the tensor cores ("3xTF32").  Each operand is
  * split into a TF32 high part and a TF32 low part (rounded to nearest), and
  * C = A_hi B_hi + A_hi B_lo + A_lo B_hi is accumulated in FP32 by tcgen05
@@ -382,7 +420,9 @@ int sgemm_device_status(cudaStream_t stream);
  * of the cluster-split launch with the plain one before it; bit 10: never
  * use the narrow tile (a forced cluster size also keeps the 128 x 128 tile);
  * bit 11: read 16-byte aligned operands through the phase maps too (every
- * shift 0), so the phased kernel can be checked on any inputs.
+ * shift 0), so the phased kernel can be checked on any inputs; bit 12:
+ * sgemm_f32_streamk takes stream-K whenever its operands allow it; bits
+ * 13..14: its grid holds that many blocks per SM (0 = one).
  * wait_limit_ns:
  * the bound of each wait
  * (default 2 s).  Affects every
