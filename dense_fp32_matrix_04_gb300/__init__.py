@@ -87,7 +87,11 @@ _SIGNATURES = {
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "sgemm_f32_host_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
-    "sgemm_debug_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
+    # test-only interface (include/sgemm_testing.h)
+    "sgemm_test_switches": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
+    "sgemm_f32_plan_model": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
+                                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lock = threading.Lock()
@@ -321,9 +325,23 @@ def sgemm_device_status(stream=None) -> int:
     return int(load().sgemm_device_status(_stream(stream)))
 
 
-def sgemm_debug_set(flags: int, wait_limit_ns: int = 2_000_000_000) -> None:
-    """Test-only switches of the library (see include/sgemm.h)."""
-    _check(load().sgemm_debug_set(int(flags), int(wait_limit_ns)), "sgemm_debug_set")
+def sgemm_test_switches(flags: int, wait_limit_ns: int = 2_000_000_000) -> None:
+    """Test-only switches of the library (include/sgemm_testing.h); they take
+    effect only in a process whose environment has SGEMM_TEST_SWITCHES=1."""
+    _check(load().sgemm_test_switches(int(flags), int(wait_limit_ns)), "sgemm_test_switches")
+
+
+PLAN_PATHS = {"tma": 0, "phased": 1, "cp": 2}
+
+
+def sgemm_f32_plan_model(M: int, N: int, K: int, sms: int, path: str = "tma"):
+    """Test-only: the plan sgemm_f32_plan reports for kernel path ``path``
+    ("tma", "phased" or "cp") on a GPU with ``sms`` SMs (every cluster size
+    assumed resident, no test switch), computed without a device."""
+    t, f, c, n = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().sgemm_f32_plan_model(int(M), int(N), int(K), PLAN_PATHS[path], int(sms), ctypes.byref(t),
+                                       ctypes.byref(f), ctypes.byref(c), ctypes.byref(n)), "sgemm_f32_plan_model")
+    return int(t.value), int(f.value), int(c.value), int(n.value)
 
 
 def _rows(t, name):

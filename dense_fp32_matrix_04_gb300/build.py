@@ -31,7 +31,7 @@ def _nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
-    files.append(os.path.join(ROOT, "include", "sgemm.h"))
+    files += [os.path.join(ROOT, "include", h) for h in ("sgemm.h", "sgemm_testing.h")]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -7,10 +7,13 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
 #include "../../include/sgemm.h"
+#include "../../include/sgemm_testing.h"
 #include "ffma_cp_packed.cuh"
 #include "ffma_tma_phased.cuh"
 #include "ffma_tma_sgemm.cuh"
@@ -45,7 +48,7 @@ using X3Tile = sgemm::Tf32x3MainTile;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 64;
 
-// test-only switches (sgemm_debug_set); bit 0 is read by the TMA kernels.
+// test-only switches (sgemm_test_switches); bit 0 is read by the TMA kernels.
 // Bit 1: route every product to the cp.async-fed kernel.  Bits 4..7: cluster
 // size forced on the cluster split of the main tile (0 = the automatic plan,
 // 1 = never split, 2 .. 8 = split the tiles beyond whole multiples of the SM
@@ -336,15 +339,19 @@ enum class Narrow { kNone, kTma, kCp, kPhased };
 // fewer main tiles than SMs, the narrow tile of the product's path (`narrow`)
 // in clusters of 2, 4 or 8 (the c with the lowest estimate, ties to the
 // larger c) is taken instead when its estimate is lower still.
-SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow, bool phased = false) {
+//
+// The model itself touches no device: `sms` is the SM count, `dbg` the
+// test-only switches, and fits(narrow, c) says whether clusters of c CTAs of
+// the narrow tile (narrow == true) or of the 128 x 128 tile can be resident.
+template <class Fits>
+SplitPlan split_plan_model(int M, int N, int K, int64_t sms, Narrow narrow, int dbg, Fits fits) {
     using T = TmaTile;
     SplitPlan plan;
     plan.tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
     plan.full = plan.tiles;
-    const int64_t P = info.sms;
+    const int64_t P = sms;
     const int64_t kt = (K + T::BK - 1) / T::BK;
     if (P <= 0 || plan.tiles == 0) return plan;
-    const int dbg = g_debug_flags.load();
     const int forced = (dbg >> kDebugClusterShift) & 15;
     const int64_t rem = plan.tiles % P;
     int64_t full = plan.tiles - rem;
@@ -369,10 +376,7 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow,
             double nbest = 0.0;
             for (int c = 2; c <= 8 && kt >= 4 * c; c *= 2) {
                 const double t = narrow_sm_time(m, (ntiles * c + P - 1) / P, (double)((kt + c - 1) / c));
-                const bool fits = narrow == Narrow::kTma      ? cluster_fits<TmaNarrow>(info.dev, c)
-                                  : narrow == Narrow::kPhased ? cluster_fits<PhasedNarrow>(info.dev, c)
-                                                              : cluster_fits<TmaNarrowCp, true>(info.dev, c);
-                if ((ncs == 0 || t <= nbest) && fits) nbest = t, ncs = c;
+                if ((ncs == 0 || t <= nbest) && fits(true, c)) nbest = t, ncs = c;
             }
             if (ncs > 0 && nbest < best) {
                 plan.tiles = ntiles;
@@ -384,10 +388,24 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow,
         }
     }
     if (cs < 2 || cs > 8 || full == plan.tiles) return plan;
-    if (!(phased ? cluster_fits<TmaPhased>(info.dev, cs) : cluster_fits<T>(info.dev, cs))) return plan;
+    if (!fits(false, cs)) return plan;
     plan.full = full;
     plan.cs = cs;
     return plan;
+}
+
+// The plan on the current device: the model with this device's SM count, the
+// test-only switches, and cluster sizes checked against the kernel of the
+// product's path.
+SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow, bool phased = false) {
+    auto fits = [&](bool narrow_tile, int c) {
+        if (narrow_tile)
+            return narrow == Narrow::kTma      ? cluster_fits<TmaNarrow>(info.dev, c)
+                   : narrow == Narrow::kPhased ? cluster_fits<PhasedNarrow>(info.dev, c)
+                                               : cluster_fits<TmaNarrowCp, true>(info.dev, c);
+        return phased ? cluster_fits<TmaPhased>(info.dev, c) : cluster_fits<TmaTile>(info.dev, c);
+    };
+    return split_plan_model(M, N, K, info.sms, narrow, g_debug_flags.load(), fits);
 }
 
 // Launch the TMA kernel over grouped tiles [tile_base, tile_base + tiles): a
@@ -917,31 +935,65 @@ int sgemm_f32(int M, int N, int K, const float *A, int lda, const float *B, int 
     return launch_product(p, 1, nullptr, 0, stream, info);
 }
 
-int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long long *full_tiles, int *cluster_size,
-                   int *tile_n) {
-    if (!tiles || !full_tiles || !cluster_size || !tile_n || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// sgemm_f32_plan's outputs for one product on path `path` (0: TMA operands,
+// 1: phased, 2: cp.async); plan_fn(narrow, phased, status) gives the split
+// plan of that path (on a device, or from the model alone).
+template <class PlanFn>
+int report_plan(int M, int N, int K, int path, PlanFn plan_fn, long long *tiles, long long *full_tiles,
+                int *cluster_size, int *tile_n) {
+    if (!tiles || !full_tiles || !cluster_size || !tile_n || M < 0 || N < 0 || K < 0 || path < 0 || path > 2)
+        return SGEMM_ERR_INVALID_ARG;
     *tiles = *full_tiles = 0;
     *cluster_size = 1;
     *tile_n = TmaTile::BN;
     if ((int64_t)M * N == 0) return SGEMM_OK;
-    DeviceInfo info;
-    if (device_info(info) != SGEMM_OK) return SGEMM_ERR_DEVICE;
-    const int dbg = g_debug_flags.load();
-    const bool cp = !tma_operands || (dbg & (kDebugForceCpAsync | kDebugForcePhased)) != 0;
-    const bool phased = cp && M >= 4 && K >= 4 && !(dbg & kDebugForceCpAsync);
-    if (K <= 2 * TmaSmallK::BK && K > 0 && !cp) {
+    if (K <= 2 * TmaSmallK::BK && K > 0 && path == 0) {
         *tiles = *full_tiles =
             (long long)((M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((N + TmaSmallK::BN - 1) / TmaSmallK::BN);
         *tile_n = TmaSmallK::BN;
         return SGEMM_OK;
     }
-    const SplitPlan plan =
-        split_plan(M, N, K, info, !cp ? Narrow::kTma : phased ? Narrow::kPhased : Narrow::kCp, phased);
+    int st = SGEMM_OK;
+    const SplitPlan plan = plan_fn(path == 0 ? Narrow::kTma : path == 1 ? Narrow::kPhased : Narrow::kCp, path == 1, st);
+    if (st != SGEMM_OK) return st;
     *tiles = plan.tiles;
     *full_tiles = plan.full;
     *cluster_size = plan.cs;
     *tile_n = plan.narrow ? TmaNarrow::BN : TmaTile::BN;
     return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long long *full_tiles, int *cluster_size,
+                   int *tile_n) {
+    const int dbg = g_debug_flags.load();
+    const bool cp = !tma_operands || (dbg & (kDebugForceCpAsync | kDebugForcePhased)) != 0;
+    const bool phased = cp && M >= 4 && K >= 4 && !(dbg & kDebugForceCpAsync);
+    auto on_device = [&](Narrow narrow, bool ph, int &st) {
+        DeviceInfo info;
+        if (device_info(info) != SGEMM_OK) {
+            st = SGEMM_ERR_DEVICE;
+            return SplitPlan{};
+        }
+        return split_plan(M, N, K, info, narrow, ph);
+    };
+    return report_plan(M, N, K, !cp ? 0 : phased ? 1 : 2, on_device, tiles, full_tiles, cluster_size, tile_n);
+}
+
+int sgemm_f32_plan_model(int M, int N, int K, int path, int sms, long long *tiles, long long *full_tiles,
+                         int *cluster_size, int *tile_n) {
+    if (sms < 1) return SGEMM_ERR_INVALID_ARG;
+    auto model = [&](Narrow narrow, bool, int &) {
+        return split_plan_model(M, N, K, sms, narrow, 0, [](bool, int) { return true; });
+    };
+    return report_plan(M, N, K, path, model, tiles, full_tiles, cluster_size, tile_n);
 }
 
 size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits) { return partials_bytes(M, N, splits); }
@@ -1440,7 +1492,9 @@ int sgemm_device_status(cudaStream_t stream) {
     return SGEMM_OK;
 }
 
-int sgemm_debug_set(int flags, unsigned long long wait_limit_ns) {
+int sgemm_test_switches(int flags, unsigned long long wait_limit_ns) {
+    const char *on = std::getenv("SGEMM_TEST_SWITCHES");
+    if (!on || std::strcmp(on, "1") != 0) return SGEMM_ERR_INVALID_ARG;
     if (flags < 0 || wait_limit_ns == 0) return SGEMM_ERR_INVALID_ARG;
     g_debug_flags.store(flags);
     g_wait_limit_ns.store(wait_limit_ns);

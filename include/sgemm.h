@@ -121,7 +121,8 @@ int sgemm_f32(int M, int N, int K,
  * cluster); 128 otherwise.  Non-TMA operands with M >= 4 and K >= 4 take the
  * phased TMA kernel's plan; smaller ones the cp.async kernel's, which assumes
  * 16 * lda and 8 * ldb fit in 32 bits (otherwise the 128 x 128 plan runs).  The result
- * reflects the test-only switches of sgemm_debug_set.  Launches nothing.
+ * reflects the switches of the test-only interface (sgemm_testing.h), which
+ * are all off unless a test turned them on.  Launches nothing.
  * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
  * if the device cannot be queried.
  */
@@ -408,28 +409,6 @@ int sgemm_f32_ladder(int level, int M, int N, int K,
  * CUDA call failed (including an earlier asynchronous error on the stream).
  */
 int sgemm_device_status(cudaStream_t stream);
-
-/*
- * TEST-ONLY.  flags bit 0: the TMA-fed kernels never issue their copies, so every
- * block's bounded wait runs out (used to check the timeout path without any
- * fault); bit 1: route every product to the cp.async kernel, so both kernels
- * can be checked on the same inputs; bits 4..7: the cluster size of the
- * cluster split, forced (0 = automatic, 1 = never split, 2 .. 8 =
- * split the tiles beyond whole multiples of the SM count with that size);
- * bit 8: with a forced size, split every tile; bit 9: no programmatic overlap
- * of the cluster-split launch with the plain one before it; bit 10: never
- * use the narrow tile (a forced cluster size also keeps the 128 x 128 tile);
- * bit 11: read 16-byte aligned operands through the phase maps too (every
- * shift 0), so the phased kernel can be checked on any inputs; bit 12:
- * sgemm_f32_streamk takes stream-K whenever its operands allow it; bits
- * 13..14: its grid holds that many blocks per SM (0 = one).
- * wait_limit_ns:
- * the bound of each wait
- * (default 2 s).  Affects every
- * later launch in this process.  SGEMM_ERR_INVALID_ARG if flags < 0 or
- * wait_limit_ns == 0.
- */
-int sgemm_debug_set(int flags, unsigned long long wait_limit_ns);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *sgemm_status_string(int status);

@@ -1,0 +1,65 @@
+/*
+ * libsgemm -- TEST-ONLY interface.
+ *
+ * Nothing here is part of the product interface in sgemm.h, and a program
+ * that computes products has no reason to include this header.  It holds the
+ * hooks that the library's own tests use to reach code paths an ordinary call
+ * never takes (a bounded wait that runs out, a kernel that the plan would not
+ * pick for these operands), and the device-free form of the launch planner.
+ */
+#ifndef SGEMM_TESTING_H
+#define SGEMM_TESTING_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Switches that change how every later product in this process is launched.
+ * They take effect only when the environment variable SGEMM_TEST_SWITCHES is
+ * "1" at the time of the call; otherwise the call changes nothing and returns
+ * SGEMM_ERR_INVALID_ARG, so a program that does not set the variable cannot
+ * turn a kernel's copies off by accident.
+ *
+ * flags bit 0: the TMA-fed kernels never issue their copies, so every block's
+ * bounded wait runs out (the timeout path, checked without any fault); bit 1:
+ * route every product to the cp.async kernel, so both kernels can be checked
+ * on the same inputs; bits 4..7: the cluster size of the cluster split,
+ * forced (0 = automatic, 1 = never split, 2 .. 8 = split the tiles beyond
+ * whole multiples of the SM count with that size); bit 8: with a forced size,
+ * split every tile; bit 9: no programmatic overlap of the cluster-split launch
+ * with the plain one before it; bit 10: never use the narrow tile (a forced
+ * cluster size also keeps the 128 x 128 tile); bit 11: read 16-byte aligned
+ * operands through the phase maps too (every shift 0), so the phased kernel
+ * can be checked on any inputs; bit 12: sgemm_f32_streamk takes stream-K
+ * whenever its operands allow it; bits 13..14: its grid holds that many blocks
+ * per SM (0 = one).
+ * wait_limit_ns: the bound of each wait (default 2 s).
+ * flags = 0 and wait_limit_ns = 2000000000 restore the defaults.
+ * SGEMM_ERR_INVALID_ARG if flags < 0, wait_limit_ns == 0, or the environment
+ * variable is not "1".
+ */
+int sgemm_test_switches(int flags, unsigned long long wait_limit_ns);
+
+/*
+ * The planner of sgemm_f32 without a device: the plan sgemm_f32_plan reports
+ * (same outputs, same meaning) for the kernel path `path` -- 0: operands the
+ * TMA can address (the TMA kernel, its small-K tile for 1 <= K <= 64);
+ * 1: operands whose rows are only 4-byte aligned, read through phase maps
+ * (sgemm_f32 takes it when M >= 4 and K >= 4); 2: the cp.async-fed kernel
+ * (which sgemm_f32 takes for the remaining unaligned products) -- computed
+ * for a GPU with `sms` SMs on which clusters of 2, 4 and 8 blocks can all be
+ * resident, with every test switch off.  It lets the cost models that choose
+ * between the plain grid, the cluster split and the narrow tile be checked
+ * on a machine without a GPU.  Launches nothing and makes no CUDA call.
+ * SGEMM_ERR_INVALID_ARG for a NULL output, a negative size, sms < 1 or an
+ * unknown path.
+ */
+int sgemm_f32_plan_model(int M, int N, int K, int path, int sms, long long *tiles, long long *full_tiles,
+                         int *cluster_size, int *tile_n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_TESTING_H */

@@ -14,14 +14,18 @@ from dense_fp32_matrix_04_gb300 import build
 HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
-def declared_functions():
+def declared_functions(headers=None):
     names = []
     for h in sorted(os.listdir(HEADER_DIR)):
-        if h.endswith(".h"):
+        if h.endswith(".h") and (headers is None or h in headers):
             text = open(os.path.join(HEADER_DIR, h)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names += re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(sgemm_\w+)\s*\(", text, flags=re.M)
     return names
+
+
+# the test-only interface lives in its own header, never in the product's
+TEST_ONLY = {"sgemm_test_switches", "sgemm_f32_plan_model"}
 
 
 @pytest.fixture(scope="module")
@@ -34,6 +38,26 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     assert "sgemm_f32" in names and "sgemm_status_string" in names
     assert len(names) == len(set(names))
+
+
+def test_product_header_has_no_test_only_symbol():
+    product = set(declared_functions({"sgemm.h"}))
+    testing = set(declared_functions({"sgemm_testing.h"}))
+    assert testing == TEST_ONLY
+    assert not product & TEST_ONLY
+    assert not any("debug" in n or "test" in n for n in product)
+
+
+def test_switches_need_the_environment(lib, monkeypatch):
+    # without SGEMM_TEST_SWITCHES=1 the call is refused and changes nothing
+    monkeypatch.delenv("SGEMM_TEST_SWITCHES", raising=False)
+    assert lib.sgemm_test_switches(1, 50_000_000) == sg.SGEMM_ERR_INVALID_ARG
+    monkeypatch.setenv("SGEMM_TEST_SWITCHES", "0")
+    assert lib.sgemm_test_switches(1, 50_000_000) == sg.SGEMM_ERR_INVALID_ARG
+    monkeypatch.setenv("SGEMM_TEST_SWITCHES", "1")
+    assert lib.sgemm_test_switches(-1, 1) == sg.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_test_switches(0, 0) == sg.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_test_switches(0, 2_000_000_000) == sg.SGEMM_OK
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -94,9 +118,9 @@ def test_empty_output_needs_no_gpu(lib):
 
 
 def test_debug_switch_validates_without_gpu(lib):
-    assert lib.sgemm_debug_set(-1, 10) == sg.SGEMM_ERR_INVALID_ARG
-    assert lib.sgemm_debug_set(0, 0) == sg.SGEMM_ERR_INVALID_ARG
-    assert lib.sgemm_debug_set(0, 2_000_000_000) == sg.SGEMM_OK
+    assert lib.sgemm_test_switches(-1, 10) == sg.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_test_switches(0, 0) == sg.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_test_switches(0, 2_000_000_000) == sg.SGEMM_OK
 
 
 def test_splitk_workspace_size(lib):

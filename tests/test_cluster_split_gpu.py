@@ -36,7 +36,7 @@ def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_device_status()
 
 
@@ -101,7 +101,7 @@ def expected_plan(M, N, K, sms, narrow="tma"):
                                         (128, 128, 288, 203)])
 def test_forced_split_matches_oracle(sg, cs, M, N, K, seed):
     A, B = gen.operands(M, N, K, seed=seed)
-    sg.sgemm_debug_set(forced(cs))
+    sg.sgemm_test_switches(forced(cs))
     tiles, full, c, tn = sg.sgemm_f32_plan(M, N, K)
     assert (full, c, tn) == (0, cs, 128)
     check_full(run_sgemm(sg, A, B), A, B)
@@ -111,14 +111,14 @@ def test_forced_split_matches_oracle(sg, cs, M, N, K, seed):
 @pytest.mark.parametrize("cs", [2, 3, 5, 8])
 def test_forced_split_integers_exact(sg, cs):
     A, B = gen.operands(256, 384, 1536, seed=204, integer_copy=True)
-    sg.sgemm_debug_set(forced(cs))
+    sg.sgemm_test_switches(forced(cs))
     check_full(run_sgemm(sg, A, B), A, B, exact=True)
 
 
 def test_ranks_without_k_steps(sg):
     # K = 100: 4 k-steps over 8 ranks, so ranks 4..7 contribute zeros
     A, B = gen.operands(200, 300, 100, seed=205)
-    sg.sgemm_debug_set(forced(8))
+    sg.sgemm_test_switches(forced(8))
     check_full(run_sgemm(sg, A, B), A, B)
 
 
@@ -127,7 +127,7 @@ def test_bitwise_repeatable(sg, cs):
     import torch
     A, B = gen.operands(512, 640, 2048, seed=206)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
-    sg.sgemm_debug_set(forced(cs))
+    sg.sgemm_test_switches(forced(cs))
     c1 = sg.matmul(dA, dB)
     c2 = sg.matmul(dA, dB)
     torch.cuda.synchronize()
@@ -139,7 +139,7 @@ def test_tail_split_after_full_waves(sg, overlap):
     # more tiles than one wave: a plain launch for the full waves, clusters for
     # the rest, with and without programmatic overlap of the two launches
     import torch
-    sg.sgemm_debug_set(0 if overlap else NO_OVERLAP)
+    sg.sgemm_test_switches(0 if overlap else NO_OVERLAP)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tiles_n = 8
     tiles_m = sms // tiles_n + 1              # one tile per SM, then a short tail
@@ -164,9 +164,9 @@ def test_automatic_plan(sg, M, N, K):
     # narrow tile runs like the TMA kernel's (four CTAs per SM) and takes its model
     assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow="tma")
     # with every product on the cp.async-fed kernel: its narrow tile and model
-    sg.sgemm_debug_set(2)
+    sg.sgemm_test_switches(2)
     assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow="cp")
-    sg.sgemm_debug_set(NO_NARROW)
+    sg.sgemm_test_switches(NO_NARROW)
     assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms, narrow=None)
     assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow=None)
 
@@ -178,7 +178,7 @@ def test_square_1024_uses_clusters_and_matches(sg):
 
 
 def test_no_split_switch(sg):
-    sg.sgemm_debug_set(NO_SPLIT)
+    sg.sgemm_test_switches(NO_SPLIT)
     tiles, full, cs, tn = sg.sgemm_f32_plan(1024, 1024, 1024)
     assert cs == 1 and full == tiles == 64 and tn == 128
 
@@ -190,7 +190,7 @@ def test_alpha_beta_with_split(sg, cs):
     A = gen.matrix(208, gen.STREAM_A, 200, 700)
     B = gen.matrix(208, gen.STREAM_B, 700, 260)
     C0 = gen.matrix(209, gen.STREAM_A, 200, 260)
-    sg.sgemm_debug_set(forced(cs))
+    sg.sgemm_test_switches(forced(cs))
     C = run_gemm(sg, 0, 0, 0, -0.75, A, B, 1.5, C0)
     C64, S, T = ref_gemm.gemm_general_f64(False, False, -0.75, A, B, 1.5, C0)
     assert tolerance.max_error_ratio_general(C, C64, S, T, 700, -0.75) <= 1.0
@@ -205,12 +205,12 @@ def test_timeout_in_cluster_mode(sg):
     A, B = gen.operands(M, N, K, seed=210)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()
-    sg.sgemm_debug_set(forced(4) | 1, 50_000_000)
+    sg.sgemm_test_switches(forced(4) | 1, 50_000_000)
     assert sg.sgemm_f32_plan(M, N, K)[2:] == (4, 128)
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
-    sg.sgemm_debug_set(forced(4))
+    sg.sgemm_test_switches(forced(4))
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)
@@ -224,7 +224,7 @@ def test_timeout_with_plain_waves_and_tail(sg):
     tiles_n = 8
     tiles_m = sms // tiles_n + 1
     M, N, K = 128 * tiles_m, 128 * tiles_n, 1024
-    sg.sgemm_debug_set(1, 50_000_000)
+    sg.sgemm_test_switches(1, 50_000_000)
     tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
     assert cs > 1 and 0 < full < tiles and tn == 128
     dA = torch.zeros(M, K, device="cuda")
@@ -233,7 +233,7 @@ def test_timeout_with_plain_waves_and_tail(sg):
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
-    sg.sgemm_debug_set(0)
+    sg.sgemm_test_switches(0)
     A, B = gen.operands(M, N, K, seed=211)
     dA.copy_(torch.from_numpy(A))
     dB.copy_(torch.from_numpy(B))

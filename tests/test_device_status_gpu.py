@@ -18,7 +18,7 @@ def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()          # start from a clear error word
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_device_status()
 
 
@@ -34,14 +34,14 @@ def test_timeout_is_reported_and_nothing_is_written(sg, K):
     A, B = gen.operands(128, 256, K, seed=31)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((128, 256), CANARY_BITS, np.int32).view(np.float32)).cuda()
-    sg.sgemm_debug_set(1, 50_000_000)     # copies never issued; 50 ms bound per wait
+    sg.sgemm_test_switches(1, 50_000_000)     # copies never issued; 50 ms bound per wait
     sg.sgemm_f32(128, 256, K, dA, K, dB, 256, dC, 256)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
     # the status is cleared by reading it
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     # and the device is still usable
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_f32(128, 256, K, dA, K, dB, 256, dC, 256)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)

@@ -24,7 +24,7 @@ def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
 
 
 def _dim(rng, hi):
@@ -72,7 +72,7 @@ def _case(sg, seed):
     ldc = N + int(rng.choice([0, 0, 3, 4]))
     a_off, b_off, c_off = (int(rng.choice([0, 0, 1, 2])) for _ in range(3))
     flags = int(rng.choice([0, 0, 1 << 4, (2 << 4) | 256, (3 << 4) | 256, (4 << 4), (8 << 4) | 256, 2, 2048]))
-    sg.sgemm_debug_set(flags)
+    sg.sgemm_test_switches(flags)
     try:
         a_buf, pa = _device_buffer(A, max(lda, 1), a_off, torch, dev)
         b_buf, pb = _device_buffer(B, max(ldb, 1), b_off, torch, dev)
@@ -101,7 +101,7 @@ def _case(sg, seed):
             assert np.isnan(w[:WS_GUARD]).all() and np.isnan(w[-WS_GUARD:]).all(), "wrote outside the workspace"
         C = _read_c(c_buf, M, N, ldc, c_off)
     finally:
-        sg.sgemm_debug_set(0)
+        sg.sgemm_test_switches(0)
     C64, S, T = ref_gemm.gemm_general_f64(bool(ta), bool(tb), alpha, A, B, beta, C0)
     r = tolerance.max_error_ratio_general(C, C64, S, T, K, alpha)
     assert r <= 1.0, f"case {seed}: {entry} {M}x{N}x{K} ta={ta} tb={tb} flags={flags}: error/bound {r:.3g}"

@@ -142,11 +142,11 @@ def test_square_1024_transposed_both(sg):
 def test_cp_async_path_with_alpha_beta(sg):
     # force the cp.async kernel (test-only switch) on the FFMA algorithm
     A, B, C0 = stored(130, 140, 150, 0, 0, seed=116)
-    sg.sgemm_debug_set(2, 2_000_000_000)
+    sg.sgemm_test_switches(2, 2_000_000_000)
     try:
         C = run_gemm(sg, 0, 0, 0, -1.25, A, B, 0.5, C0)
     finally:
-        sg.sgemm_debug_set(0, 2_000_000_000)
+        sg.sgemm_test_switches(0, 2_000_000_000)
     check_general(C, 0, 0, -1.25, A, B, 0.5, C0)
 
 

@@ -53,12 +53,12 @@ NO_SPLIT = 1 << 4
 def test_equals_sgemm_f32(sg, panels):
     A, B = gen.operands(1000, 520, 300, seed=120)
     check_full(host_product(sg, A, B, panels), A, B)
-    sg.sgemm_debug_set(NO_SPLIT)
+    sg.sgemm_test_switches(NO_SPLIT)
     try:
         C = host_product(sg, A, B, panels)
         assert np.array_equal(C, device_product(sg, A, B))
     finally:
-        sg.sgemm_debug_set(0)
+        sg.sgemm_test_switches(0)
 
 
 def test_several_panels_and_column_blocks(sg):
@@ -72,11 +72,11 @@ def test_several_panels_and_column_blocks(sg):
     rows = [0, 1, 127, 128, M // 2, M - 78, M - 77, M - 1] + list(np.random.default_rng(2).integers(0, M, 10))
     from helpers import check_rows
     check_rows(C, A, B, rows)
-    sg.sgemm_debug_set(NO_SPLIT)
+    sg.sgemm_test_switches(NO_SPLIT)
     try:
         assert np.array_equal(host_product(sg, A, B, 3), device_product(sg, A, B))
     finally:
-        sg.sgemm_debug_set(0)
+        sg.sgemm_test_switches(0)
 
 
 def test_strides_and_ragged(sg):

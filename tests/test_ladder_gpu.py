@@ -110,9 +110,9 @@ def test_product_kernels_equal_the_naive_kernel_bitwise(sg, path, flags, pad, M,
     ldb = (N + 3) // 4 * 4 if pad == 4 else N + pad
     naive = run_ladder(sg, 0, A, B, lda=lda, ldb=ldb)
     from helpers import run_sgemm
-    sg.sgemm_debug_set(flags)
+    sg.sgemm_test_switches(flags)
     try:
         C = run_sgemm(sg, A, B, lda=lda, ldb=ldb)
     finally:
-        sg.sgemm_debug_set(0)
+        sg.sgemm_test_switches(0)
     assert np.array_equal(C, naive), f"{path}: {np.count_nonzero(C != naive)} outputs differ from the naive kernel"

@@ -24,7 +24,7 @@ def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_device_status()
 
 
@@ -83,7 +83,7 @@ def test_against_the_wide_tile(sg):
     narrow_plan(sg, M, N, K)
     A, B = gen.operands(M, N, K, seed=622)
     c_narrow = run_sgemm(sg, A, B)
-    sg.sgemm_debug_set(NO_NARROW)
+    sg.sgemm_test_switches(NO_NARROW)
     assert sg.sgemm_f32_plan(M, N, K)[3] == 128
     c_wide = run_sgemm(sg, A, B)
     check_full(c_narrow, A, B)
@@ -112,11 +112,11 @@ def test_timeout(sg):
     A, B = gen.operands(M, N, K, seed=625)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()
-    sg.sgemm_debug_set(1, 50_000_000)
+    sg.sgemm_test_switches(1, 50_000_000)
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
-    sg.sgemm_debug_set(0)
+    sg.sgemm_test_switches(0)
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)
@@ -134,7 +134,7 @@ def test_timeout(sg):
                                                (300, 190, 999, 4, 2)])   # A 16-byte, B 4-byte, ragged
 def test_cp_matches_oracle(sg, M, N, K, pad_a, pad_b):
     # rows of A and B padded so that at least one operand is not TMA-addressable
-    sg.sgemm_debug_set(FORCE_CP)
+    sg.sgemm_test_switches(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=630 + M % 89)
     lda = ld4(K) + 4 if pad_a == 4 else K + pad_a      # pad 4: rows 16-byte aligned
@@ -145,7 +145,7 @@ def test_cp_matches_oracle(sg, M, N, K, pad_a, pad_b):
 
 def test_cp_unaligned_base(sg):
     M, N, K = 384, 320, 1500
-    sg.sgemm_debug_set(FORCE_CP)
+    sg.sgemm_test_switches(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=640)
     check_full(run_sgemm(sg, A, B, a_off=1, b_off=2, c_off=3), A, B)
@@ -153,7 +153,7 @@ def test_cp_unaligned_base(sg):
 
 def test_cp_wide_grid_sampled(sg):
     M, N, K = 2048, 1024, 2048
-    sg.sgemm_debug_set(FORCE_CP)
+    sg.sgemm_test_switches(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=641)
     C = run_sgemm(sg, A, B, lda=K + 1, ldb=N + 1)
@@ -164,7 +164,7 @@ def test_cp_wide_grid_sampled(sg):
 def test_cp_integers_exact_and_repeatable(sg):
     import torch
     M, N, K = 384, 320, 1537
-    sg.sgemm_debug_set(FORCE_CP)
+    sg.sgemm_test_switches(FORCE_CP)
     narrow_plan(sg, M, N, K, aligned=False)
     A, B = gen.operands(M, N, K, seed=642, integer_copy=True)
     c1 = run_sgemm(sg, A, B)

@@ -25,9 +25,9 @@ def path(request, sg):
     cp.async kernel, and again with aligned operands read through the phase
     maps of the phased TMA kernel (test-only switches)."""
     flags = {"auto": 0, "no-cluster-split": 1 << 4, "cp.async": 2, "phased": 2048}[request.param]
-    sg.sgemm_debug_set(flags, 2_000_000_000)
+    sg.sgemm_test_switches(flags, 2_000_000_000)
     yield request.param
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
 
 
 # ------------------------------------------------------------------ the workloads

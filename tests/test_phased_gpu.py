@@ -31,9 +31,9 @@ def forced(cs):
 def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_device_status()
 
 
@@ -43,7 +43,7 @@ def sg(cuda_device, lib):
 @pytest.mark.parametrize("b_off,ldb_pad", [(0, 0), (0, 1), (2, 2), (3, 1)])
 def test_every_shift_pattern(sg, a_off, lda_pad, b_off, ldb_pad):
     M, N, K = 261, 259, 101          # two and a bit tiles each way, a partial last k-step
-    sg.sgemm_debug_set(NO_NARROW)
+    sg.sgemm_test_switches(NO_NARROW)
     A, B = gen.operands(M, N, K, seed=400 + 7 * a_off + lda_pad)
     C = run_sgemm(sg, A, B, lda=K + lda_pad, ldb=N + ldb_pad, a_off=a_off, b_off=b_off)
     check_full(C, A, B)
@@ -55,7 +55,7 @@ def test_every_shift_pattern(sg, a_off, lda_pad, b_off, ldb_pad):
 @pytest.mark.parametrize("M,N,K", [(4, 4, 4), (5, 7, 4), (4, 300, 37), (300, 4, 5), (127, 129, 31), (128, 128, 32),
                                    (129, 1, 1000), (7, 513, 65)])
 def test_small_and_edge_shapes(sg, M, N, K):
-    sg.sgemm_debug_set(NO_NARROW)
+    sg.sgemm_test_switches(NO_NARROW)
     A, B = gen.operands(M, N, K, seed=410)
     check_full(run_sgemm(sg, A, B, lda=K + 1, ldb=N + 3, a_off=2, b_off=1), A, B)
 
@@ -69,7 +69,7 @@ def test_fewer_than_four_rows_take_the_cp_async_kernel(sg, M, N, K):
 def test_aligned_operands_through_the_phase_maps(sg):
     # a test-only switch routes 16-byte aligned operands here too (every shift 0)
     A, B = gen.operands(300, 520, 200, seed=412)
-    sg.sgemm_debug_set(FORCE_PHASED | NO_NARROW)
+    sg.sgemm_test_switches(FORCE_PHASED | NO_NARROW)
     check_full(run_sgemm(sg, A, B), A, B)
     Ai, Bi = gen.operands(300, 520, 200, seed=412, integer_copy=True)
     check_full(run_sgemm(sg, Ai, Bi), Ai, Bi, exact=True)
@@ -79,7 +79,7 @@ def test_aligned_operands_through_the_phase_maps(sg):
 def test_cluster_split(sg, cs):
     M, N, K = 300, 260, 777
     A, B = gen.operands(M, N, K, seed=420 + cs)
-    sg.sgemm_debug_set(forced(cs))
+    sg.sgemm_test_switches(forced(cs))
     assert sg.sgemm_f32_plan(M, N, K, aligned=False)[2] == cs
     C1 = run_sgemm(sg, A, B, lda=K + 3, ldb=N + 1, a_off=1, b_off=3)
     check_full(C1, A, B)
@@ -125,13 +125,13 @@ def test_timeout_is_reported_and_nothing_is_written(sg, flags):
     a_buf, pa = _device_buffer(A, K + 1, 1, torch, dev)
     b_buf, pb = _device_buffer(B, N + 3, 0, torch, dev)
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()
-    sg.sgemm_debug_set(flags | 1, 50_000_000)
+    sg.sgemm_test_switches(flags | 1, 50_000_000)
     assert sg.sgemm_f32_plan(M, N, K, aligned=False)[3] == (64 if flags == 0 else 128)
     sg.sgemm_f32(M, N, K, pa, K + 1, pb, N + 3, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
-    sg.sgemm_debug_set(flags, 2_000_000_000)
+    sg.sgemm_test_switches(flags, 2_000_000_000)
     sg.sgemm_f32(M, N, K, pa, K + 1, pb, N + 3, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)

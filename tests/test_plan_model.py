@@ -1,0 +1,131 @@
+"""The launch planner's fitted cost models, checked on the CPU against the
+plans measured fastest on a GB300 (152 SMs).
+
+sgemm_f32 chooses, per product, between a plain grid of 128 x 128 tiles, the
+same grid with its last partial round of tiles split over thread-block
+clusters, and (with fewer main tiles than SMs) narrow 128 x 64 tiles in
+clusters.  The choice comes from cost models fitted to timings; the tables
+below are those timings (TFLOP/s, CUDA events, medians) and the test asks the
+device-free planner (sgemm_f32_plan_model) for each shape.  The rule: the
+planner picks the plan measured fastest, or one measured within 2 % of it
+(the spread between repeated runs of the same plan on these shapes).
+"""
+
+import pytest
+
+import dense_fp32_matrix_04_gb300 as sg
+from dense_fp32_matrix_04_gb300 import build
+
+SMS = 152
+NEAR = 0.02
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    sg.load()
+
+
+# The 128 x 128 tile (TMA path) with the cluster split of its last partial
+# round of tiles: shape -> (full tiles, cluster size) of the faster plan, with
+# the measured rates of the plain grid and of that split.
+SPLIT_MEASURED = [
+    # M, N, K, (full, cs) measured fastest, plain TF/s, split TF/s
+    (2048, 2048, 2048, (152, 4), 51.8, 58.1),
+    (2560, 2560, 4096, (304, 4), 56.1, 61.3),
+    (3008, 5008, 2048, (912, 8), 56.2, 61.0),
+    (4955, 1020, 1024, (304, 8), 42.0, 58.0),
+    (6144, 6144, 6144, (2280, 8), 62.9, 65.1),
+]
+
+# Shapes whose split measured within 0.3 % of the plain grid: the plain grid
+# (no split) is the plan.
+NO_SPLIT = [(8192, 8192, 8192), (4096, 4096, 4096), (3072, 3072, 3072), (5120, 5120, 5120), (7168, 7168, 7168),
+            (896, 8192, 8192)]
+
+# Fewer main tiles than SMs: the 128 x 128 plan against the narrow-tile plan
+# (TFLOP/s), TMA operands and operands read by the cp.async kernel
+# (lda = K + 1, ldb = N + 1).
+NARROW_TMA = [
+    (512, 512, 512, 11.1, 15.7),
+    (512, 512, 4096, 22.5, 39.1),
+    (768, 768, 768, 29.6, 31.8),
+    (1024, 1024, 1024, 38.1, 40.0),
+    (1024, 1024, 8192, 50.1, 50.7),
+    (1280, 1280, 1280, 44.8, 45.4),
+    (1536, 1536, 1536, 52.8, 52.0),
+    (2048, 1024, 2048, 47.7, 54.5),
+    (1000, 2000, 4096, 46.7, 54.7),
+    (640, 640, 8192, 37.6, 48.8),
+]
+NARROW_CP = [
+    (512, 512, 512, 7.5, 14.1),
+    (512, 512, 4096, 19.1, 31.6),
+    (768, 768, 768, 20.7, 27.0),
+    (1024, 1024, 1024, 33.1, 33.6),
+    (1536, 1536, 1536, 35.4, 42.6),
+    (2048, 1024, 2048, 32.6, 44.7),
+    (1000, 2000, 4096, 31.5, 45.2),
+    (640, 640, 8192, 30.7, 39.4),
+]
+
+
+def tiles128(M, N):
+    return -(-M // 128) * -(-N // 128)
+
+
+@pytest.mark.parametrize("M,N,K,best,plain,split", SPLIT_MEASURED)
+def test_cluster_split_plan_is_the_measured_fastest(M, N, K, best, plain, split):
+    tiles, full, cs, tile_n = sg.sgemm_f32_plan_model(M, N, K, SMS, "tma")
+    assert split > plain
+    assert (tiles, tile_n) == (tiles128(M, N), 128)
+    assert (full, cs) == best
+
+
+@pytest.mark.parametrize("M,N,K", NO_SPLIT)
+def test_no_split_where_it_does_not_pay(M, N, K):
+    assert sg.sgemm_f32_plan_model(M, N, K, SMS, "tma") == (tiles128(M, N), tiles128(M, N), 1, 128)
+
+
+@pytest.mark.parametrize("path,row", [("tma", r) for r in NARROW_TMA] + [("cp", r) for r in NARROW_CP])
+def test_narrow_tile_choice_matches_the_measurements(path, row):
+    M, N, K, wide, narrow = row
+    assert tiles128(M, N) < SMS
+    tiles, full, cs, tile_n = sg.sgemm_f32_plan_model(M, N, K, SMS, path)
+    picked = narrow if tile_n == 64 else wide
+    assert picked >= (1 - NEAR) * max(wide, narrow), (
+        f"{M}x{N}x{K} on {path}: planned {'narrow' if tile_n == 64 else '128x128'} ({picked} TF/s) "
+        f"against {max(wide, narrow)} TF/s measured for the other plan")
+    if tile_n == 64:
+        # the narrow tile always runs as clusters that split each tile's k-steps
+        assert full == 0 and cs in (2, 4, 8) and tiles == -(-M // 128) * -(-N // 64)
+
+
+def test_narrow_tile_needs_fewer_main_tiles_than_sms():
+    # 2048 x 2048 x 512 has 256 main tiles: the narrow tile is not considered
+    assert sg.sgemm_f32_plan_model(2048, 2048, 512, SMS, "tma") == (256, 256, 1, 128)
+
+
+def test_small_k_tile_for_tma_operands_only():
+    # 1 <= K <= 64 with TMA operands: the 128 x 64 small-K tile, never split
+    assert sg.sgemm_f32_plan_model(16384, 16384, 32, SMS, "tma") == (32768, 32768, 1, 64)
+    assert sg.sgemm_f32_plan_model(16384, 16384, 64, SMS, "tma") == (32768, 32768, 1, 64)
+    # the same product through the phase maps takes the 128 x 128 tile
+    assert sg.sgemm_f32_plan_model(16384, 16384, 32, SMS, "phased") == (16384, 16384, 1, 128)
+
+
+def test_the_plan_follows_the_sm_count():
+    # one full round on 152 SMs is a partial one on 148
+    assert sg.sgemm_f32_plan_model(2432, 1024, 4096, SMS, "tma") == (152, 152, 1, 128)
+    tiles, full, cs, _ = sg.sgemm_f32_plan_model(2432, 1024, 4096, 148, "tma")
+    assert tiles == 152 and full == 148 and cs > 1
+
+
+@pytest.mark.parametrize("args", [(-1, 4, 4, SMS, 0), (4, 4, 4, 0, 0), (4, 4, 4, SMS, 3), (4, 4, 4, SMS, -1)])
+def test_model_rejects_bad_arguments(args):
+    import ctypes
+    M, N, K, sms, path = args
+    t, f, c, n = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_int(), ctypes.c_int()
+    st = sg.load().sgemm_f32_plan_model(M, N, K, path, sms, ctypes.byref(t), ctypes.byref(f), ctypes.byref(c),
+                                        ctypes.byref(n))
+    assert st == sg.SGEMM_ERR_INVALID_ARG

@@ -20,7 +20,7 @@ def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_device_status()
 
 
@@ -58,7 +58,7 @@ def test_bitwise_equal_to_the_main_tile(sg, K):
     dA.copy_(torch.from_numpy(A))
     dB = torch.from_numpy(B).cuda()
     c1 = sg.matmul(dA, dB)
-    sg.sgemm_debug_set(FORCE_CP_ASYNC)
+    sg.sgemm_test_switches(FORCE_CP_ASYNC)
     c2 = sg.matmul(dA, dB)
     torch.cuda.synchronize()
     assert torch.equal(c1, c2)
@@ -83,11 +83,11 @@ def test_timeout_with_many_ctas(sg, K):
     A, B = gen.operands(M, N, K, seed=314)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()
-    sg.sgemm_debug_set(1, 50_000_000)
+    sg.sgemm_test_switches(1, 50_000_000)
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
-    sg.sgemm_debug_set(0)
+    sg.sgemm_test_switches(0)
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_rows(dC.cpu().numpy(), A, B, [0, 1000, M - 1])

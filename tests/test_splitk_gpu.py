@@ -19,9 +19,9 @@ def sg(cuda_device, lib):
 
 @pytest.fixture(params=["auto", "cp.async"])
 def path(request, sg):
-    sg.sgemm_debug_set(2 if request.param == "cp.async" else 0, 2_000_000_000)
+    sg.sgemm_test_switches(2 if request.param == "cp.async" else 0, 2_000_000_000)
     yield request.param
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
 
 
 def test_square_1024_suggested_split(sg, path):

@@ -24,7 +24,7 @@ def sg(cuda_device, lib):
     import dense_fp32_matrix_04_gb300 as sg
     sg.sgemm_device_status()
     yield sg
-    sg.sgemm_debug_set(0, 2_000_000_000)
+    sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_device_status()
 
 
@@ -75,7 +75,7 @@ def test_planned_long_k_shapes(sg, M, N, K):
 
 @pytest.fixture(params=["one-per-sm", "two-per-sm"])
 def forced(request, sg):
-    sg.sgemm_debug_set(FORCE_STREAMK | (TWO_PER_SM if request.param == "two-per-sm" else 0))
+    sg.sgemm_test_switches(FORCE_STREAMK | (TWO_PER_SM if request.param == "two-per-sm" else 0))
     return request.param
 
 
@@ -166,11 +166,11 @@ def test_timeout_writes_nothing(sg):
     dC = torch.from_numpy(np.full((M, N), CANARY_BITS, np.int32).view(np.float32)).cuda()
     need = sg.sgemm_f32_streamk_workspace_size(M, N, K)
     ws = torch.empty(need // 4, device="cuda")
-    sg.sgemm_debug_set(1, 50_000_000)
+    sg.sgemm_test_switches(1, 50_000_000)
     sg.sgemm_f32_streamk(M, N, K, dA, K, dB, N, dC, N, ws, need)
     assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
-    sg.sgemm_debug_set(0)
+    sg.sgemm_test_switches(0)
     sg.sgemm_f32_streamk(M, N, K, dA, K, dB, N, dC, N, ws, need)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)

@@ -136,12 +136,12 @@ def test_timeout_path(sg):
     need = sg.sgemm_f32_3xtf32_workspace_size(128, 256, 64)
     ws = torch.empty(need // 4, device="cuda")
     try:
-        sg.sgemm_debug_set(1, 50_000_000)
+        sg.sgemm_test_switches(1, 50_000_000)
         sg.sgemm_f32_3xtf32(128, 256, 64, dA, 64, dB, 256, dC, 256, ws, need)
         assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
         assert np.all(dC.cpu().numpy().view(np.int32) == CANARY_BITS)
     finally:
-        sg.sgemm_debug_set(0, 2_000_000_000)
+        sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_f32_3xtf32(128, 256, 64, dA, 64, dB, 256, dC, 256, ws, need)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)
@@ -215,11 +215,11 @@ def test_divided_product_timeout_reports(sg):
     assert need > _operand_bytes(M, N, K)
     ws = torch.empty(need // 4, device="cuda")
     try:
-        sg.sgemm_debug_set(1, 50_000_000)
+        sg.sgemm_test_switches(1, 50_000_000)
         sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, need)
         assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     finally:
-        sg.sgemm_debug_set(0, 2_000_000_000)
+        sg.sgemm_test_switches(0, 2_000_000_000)
     sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, need)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)

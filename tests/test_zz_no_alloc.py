@@ -109,14 +109,14 @@ def test_noalloc_timeout_leaves_no_stale_partials_in_c(cuda_device, lib):
     A, B = gen.operands(M, N, K, seed=65)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     dC = torch.zeros((M, N), device="cuda")
-    sg.sgemm_debug_set(1, 50_000_000)
+    sg.sgemm_test_switches(1, 50_000_000)
     try:
         st = lib.sgemm_f32_splitk_noalloc(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N, splits,
                                           torch.cuda.current_stream().cuda_stream)
         assert st == sg.SGEMM_OK
         assert sg.sgemm_device_status() == sg.SGEMM_ERR_TIMEOUT
     finally:
-        sg.sgemm_debug_set(0, 2_000_000_000)
+        sg.sgemm_test_switches(0, 2_000_000_000)
     assert bool(torch.isnan(dC).all())
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     # and the next call is correct again
