@@ -731,9 +731,10 @@ def run_ours(args):
                     "peak_basis": TF32_PEAK_NOTE.format(tsrc=tsrc), "traffic": None,
                     "tensor_pipe_active_ncu": recorded_tensor_pipe(args.workload),
                     "algorithmic_bytes": alg_bytes,
-                    "kernel": "split kernels + sgemm_3xtf32_kernel (tcgen05 kind::tf32, 128x256 tiles, 3 MMAs "
-                              "per k-slice); achieved counts the 3 TF32 products per FP32 product over the whole "
-                              "step, split passes included"}
+                    "kernel": "split kernels + sgemm_3xtf32_kernel (tcgen05 kind::tf32, persistent, one CTA per "
+                              "SM, 128x208 tiles (192..128 where they fill the last round better), 5-stage TMA ring, "
+                              "two TMEM accumulators, 3 MMAs per k-slice); achieved counts the 3 TF32 products per "
+                              "FP32 product over the whole step, split passes included"}
         roofline["frac"] = roofline["achieved"] / tpk
     if clocks.get("sm_mhz") and roofline["bound"] == "alu":
         p = sms * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12

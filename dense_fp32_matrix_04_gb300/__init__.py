@@ -92,6 +92,8 @@ _SIGNATURES = {
     "sgemm_f32_plan_model": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
                                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "sgemm_f32_3xtf32_plan_model": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lock = threading.Lock()
@@ -342,6 +344,15 @@ def sgemm_f32_plan_model(M: int, N: int, K: int, sms: int, path: str = "tma"):
     _check(load().sgemm_f32_plan_model(int(M), int(N), int(K), PLAN_PATHS[path], int(sms), ctypes.byref(t),
                                        ctypes.byref(f), ctypes.byref(c), ctypes.byref(n)), "sgemm_f32_plan_model")
     return int(t.value), int(f.value), int(c.value), int(n.value)
+
+
+def sgemm_f32_3xtf32_plan_model(M: int, N: int, K: int, sms: int):
+    """Test-only: (tile width, k-splits) of sgemm_f32_3xtf32 for an M x N x K
+    product on a GPU with ``sms`` SMs, computed without a device."""
+    w, s = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().sgemm_f32_3xtf32_plan_model(int(M), int(N), int(K), int(sms), ctypes.byref(w), ctypes.byref(s)),
+           "sgemm_f32_3xtf32_plan_model")
+    return int(w.value), int(s.value)
 
 
 def _rows(t, name):

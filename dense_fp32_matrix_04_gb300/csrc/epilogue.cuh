@@ -35,6 +35,12 @@ __device__ __forceinline__ void store_quad(float *crow, int col, int N, const fl
     }
 }
 
+// The same arithmetic for one element: C = alpha * v (beta == 0, C not read)
+// or alpha * v + beta * C rounded once.
+__device__ __forceinline__ void store_one(float *c, float v, float alpha, float beta) {
+    *c = beta == 0.f ? alpha * v : fmaf(alpha, v, beta * *c);
+}
+
 // C = beta * C over an M x N block (C = 0 when beta == 0, without reading C):
 // the whole product when alpha == 0 or K == 0 leaves nothing to multiply.
 __global__ void __launch_bounds__(256) scale_kernel(int M, int N, float beta, float *__restrict__ C, int ldc) {

@@ -798,14 +798,15 @@ size_t partials_bytes(int M, int N, int splits) {
 // Row length of the split operands in the 3xTF32 workspace (16-byte rows for TMA).
 int64_t x3_kpad(int K) { return ((int64_t)K + 3) / 4 * 4; }
 
-// Split count of the 3xTF32 product: its kernel runs one CTA per SM, so a grid
-// of fewer than half as many 128 x 256 tiles as SMs has its k-steps divided
-// among CTA rows (up to 16, keeping at least eight 16-deep k-steps each), and
-// the partial tiles are added in row order by the split-K reduction.
-int x3_splits(int M, int N, int K, int sms) {
+// Split count of the 3xTF32 product on 128 x bn tiles: its kernel runs one
+// CTA per SM, so a grid of fewer than half as many tiles as SMs has its
+// k-steps divided among CTA rows (up to 16, keeping at least eight 16-deep
+// k-steps each), and the partial tiles are added in row order by the split-K
+// reduction.
+int x3_splits(int M, int N, int K, int sms, int bn) {
     using T = X3Tile;
     if (M <= 0 || N <= 0 || K <= 0 || sms <= 0) return 1;
-    const int64_t tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
+    const int64_t tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + bn - 1) / bn);
     const int64_t kt = (K + T::BK - 1) / T::BK;
     if (2 * tiles > sms) return 1;
     int64_t s = sms / tiles;
@@ -816,6 +817,30 @@ int x3_splits(int M, int N, int K, int sms) {
     return (int)((kt + per - 1) / per);
 }
 
+// Tile width of the 3xTF32 product.  With one CTA per SM, a grid of T tiles
+// takes ceil(T / sms) rounds, and a round of 128 x w tiles costs about
+// (w + 128) units: the copies of a k-step move 128 rows of A (hi and lo)
+// whatever the width, and w rows of B.  Fitted to the sweep on GB300 (GEMM
+// alone): against the 208-wide tile, 192 is predicted 1.06x / 1.19x slower at
+// 8192^3 / 3001 x 4999 x 2047 and measured 1.05x / 1.17x; 160 predicted
+// 1.11x / 1.29x, measured 1.12x / 1.29x.  The width with the fewest units
+// wins, ties to the wider tile; grids small enough for the split-K rows keep
+// the main (208-wide) tile.
+int x3_width(int M, int N, int sms) {
+    using T = X3Tile;
+    if (M <= 0 || N <= 0 || sms <= 0) return T::BN;
+    const int64_t tm = (M + T::BM - 1) / T::BM;
+    if (2 * tm * ((N + T::BN - 1) / T::BN) <= sms) return T::BN;
+    int best = T::BN;
+    int64_t best_cost = -1;
+    for (int bn : sgemm::kTf32x3Widths) {
+        const int64_t rounds = (tm * ((N + bn - 1) / bn) + sms - 1) / sms;
+        const int64_t cost = rounds * (bn + 128);
+        if (best_cost < 0 || cost < best_cost) best = bn, best_cost = cost;
+    }
+    return best;
+}
+
 int64_t up256(int64_t b) { return (b + 255) / 256 * 256; }
 
 // Workspace of a 3xTF32 product: the split operands (A_hi, A_lo: M x K_pad;
@@ -823,7 +848,7 @@ int64_t up256(int64_t b) { return (b + 255) / 256 * 256; }
 size_t x3_workspace_bytes(int M, int N, int K, int sms) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     const int64_t ops = 4 * x3_kpad(K) * (2 * (int64_t)M + 2 * (int64_t)N);
-    return (size_t)(up256(ops) + (int64_t)partials_bytes(M, N, x3_splits(M, N, K, sms)));
+    return (size_t)(up256(ops) + (int64_t)partials_bytes(M, N, x3_splits(M, N, K, sms, x3_width(M, N, sms))));
 }
 
 int device_sms() {
@@ -831,10 +856,49 @@ int device_sms() {
     return device_info(info) == SGEMM_OK ? info.sms : 0;
 }
 
-// The four launches of a 3xTF32 product: split A, split and transpose B, then
-// the tensor-core kernel over 128 x 256 output tiles.
+// The tensor-core part of a 3xTF32 product on 128 x T::BN tiles, from the
+// split operands ah, al (M x kp) and bh, bl (N x kp); `partials` is the
+// workspace after them.
+template <class T>
+int launch_3xtf32_gemm(const Problem &p, const float *ah, const float *al, const float *bh, const float *bl,
+                       int64_t kp, float *partials, cudaStream_t stream, const DeviceInfo &info) {
+    alignas(64) CUtensorMap tah, tal, tbh, tbl;
+    const CUtensorMapSwizzle sw = T::ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_2d(&tah, ah, p.M, p.K, (int)kp, T::BM, T::BK, sw) ||
+        !encode_2d(&tal, al, p.M, p.K, (int)kp, T::BM, T::BK, sw) ||
+        !encode_2d(&tbh, bh, p.N, p.K, (int)kp, T::BN, T::BK, sw) ||
+        !encode_2d(&tbl, bl, p.N, p.K, (int)kp, T::BN, T::BK, sw))
+        return SGEMM_ERR_LAUNCH;
+    const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
+    static std::atomic<int> done_v[kMaxDevices], done_s[kMaxDevices];
+    if (!smem_attr_once(done_v[info.dev], sgemm::sgemm_3xtf32_kernel<T, true>, T::SMEM_BYTES) ||
+        (!vc && !smem_attr_once(done_s[info.dev], sgemm::sgemm_3xtf32_kernel<T, false>, T::SMEM_BYTES)))
+        return SGEMM_ERR_LAUNCH;
+    auto kernel = vc ? sgemm::sgemm_3xtf32_kernel<T, true> : sgemm::sgemm_3xtf32_kernel<T, false>;
+    const int64_t tiles = (int64_t)((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN);
+    const int splits = x3_splits(p.M, p.N, p.K, info.sms, T::BN);
+    // persistent: one CTA per SM (at most one per unit) walks the tiles x splits units
+    const int64_t units = tiles * splits;
+    const unsigned grid = (unsigned)(units < info.sms ? units : info.sms);
+    const int ldp = ld_partials(p.N);
+    if (splits > 1) {
+        // the kernel writes raw partial tiles; alpha and beta act in the reduction
+        sgemm::sgemm_3xtf32_kernel<T, true><<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(
+            tah, tal, tbh, tbl, p.M, p.N, p.K, splits, 1.f, 0.f, partials, ldp, partials, ldp, info.err_word,
+            g_wait_limit_ns.load(), g_debug_flags.load());
+        if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
+        return launch_reduce(p, splits, partials, ldp, stream, info);
+    }
+    kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(tah, tal, tbh, tbl, p.M, p.N, p.K, 1, p.alpha, p.beta, p.C,
+                                                        p.ldc, nullptr, 0, info.err_word, g_wait_limit_ns.load(),
+                                                        g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+// The launches of a 3xTF32 product: split A, split and transpose B, then the
+// tensor-core kernel over 128 x w output tiles (w from x3_width), and for
+// small grids the split-K reduction.
 int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const DeviceInfo &info) {
-    using T = X3Tile;
     const int64_t kp = x3_kpad(p.K);
     float *ah = ws, *al = ws + (int64_t)p.M * kp;
     float *bh = al + (int64_t)p.M * kp, *bl = bh + (int64_t)p.N * kp;
@@ -856,35 +920,15 @@ int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const Device
     if (p.transb) split_rows(p.N, p.B, p.ldb, bh, bl);        // B stored N x K
     else split_transposed(p.N, p.B, p.ldb, bh, bl);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    alignas(64) CUtensorMap tah, tal, tbh, tbl;
-    const CUtensorMapSwizzle sw = T::ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!encode_2d(&tah, ah, p.M, p.K, (int)kp, T::BM, T::BK, sw) ||
-        !encode_2d(&tal, al, p.M, p.K, (int)kp, T::BM, T::BK, sw) ||
-        !encode_2d(&tbh, bh, p.N, p.K, (int)kp, T::BN, T::BK, sw) ||
-        !encode_2d(&tbl, bl, p.N, p.K, (int)kp, T::BN, T::BK, sw))
-        return SGEMM_ERR_LAUNCH;
-    const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
-    static std::atomic<int> done_v[kMaxDevices], done_s[kMaxDevices];
-    if (!smem_attr_once(done_v[info.dev], sgemm::sgemm_3xtf32_kernel<T, true>, T::SMEM_BYTES) ||
-        (!vc && !smem_attr_once(done_s[info.dev], sgemm::sgemm_3xtf32_kernel<T, false>, T::SMEM_BYTES)))
-        return SGEMM_ERR_LAUNCH;
-    auto kernel = vc ? sgemm::sgemm_3xtf32_kernel<T, true> : sgemm::sgemm_3xtf32_kernel<T, false>;
-    const unsigned tiles = (unsigned)(((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN));
-    const int splits = x3_splits(p.M, p.N, p.K, info.sms);
     float *partials = ws + up256(4 * kp * (2 * (int64_t)p.M + 2 * (int64_t)p.N)) / 4;
-    const int ldp = ld_partials(p.N);
-    if (splits > 1) {
-        // the kernel writes raw partial tiles; alpha and beta act in the reduction
-        sgemm::sgemm_3xtf32_kernel<T, true><<<dim3(tiles, (unsigned)splits), T::THREADS, T::SMEM_BYTES, stream>>>(
-            tah, tal, tbh, tbl, p.M, p.N, p.K, 1.f, 0.f, partials, ldp, partials, ldp, info.err_word,
-            g_wait_limit_ns.load(), g_debug_flags.load());
-        if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
-        return launch_reduce(p, splits, partials, ldp, stream, info);
+    switch (x3_width(p.M, p.N, info.sms)) {
+        case 192: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<192>>(p, ah, al, bh, bl, kp, partials, stream, info);
+        case 176: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<176>>(p, ah, al, bh, bl, kp, partials, stream, info);
+        case 160: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<160>>(p, ah, al, bh, bl, kp, partials, stream, info);
+        case 144: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<144>>(p, ah, al, bh, bl, kp, partials, stream, info);
+        case 128: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<128>>(p, ah, al, bh, bl, kp, partials, stream, info);
+        default: return launch_3xtf32_gemm<X3Tile>(p, ah, al, bh, bl, kp, partials, stream, info);
     }
-    kernel<<<tiles, T::THREADS, T::SMEM_BYTES, stream>>>(tah, tal, tbh, tbl, p.M, p.N, p.K, p.alpha, p.beta, p.C, p.ldc,
-                                                         nullptr, 0, info.err_word, g_wait_limit_ns.load(),
-                                                         g_debug_flags.load());
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
 // Device address of g_splitk_noalloc_scratch on the current device, looked up
@@ -985,6 +1029,13 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
         return split_plan(M, N, K, info, narrow, ph);
     };
     return report_plan(M, N, K, !cp ? 0 : phased ? 1 : 2, on_device, tiles, full_tiles, cluster_size, tile_n);
+}
+
+int sgemm_f32_3xtf32_plan_model(int M, int N, int K, int sms, int *tile_n, int *splits) {
+    if (!tile_n || !splits || M < 0 || N < 0 || K < 0 || sms < 1) return SGEMM_ERR_INVALID_ARG;
+    *tile_n = x3_width(M, N, sms);
+    *splits = x3_splits(M, N, K, sms, *tile_n);
+    return SGEMM_OK;
 }
 
 int sgemm_f32_plan_model(int M, int N, int K, int path, int sms, long long *tiles, long long *full_tiles,

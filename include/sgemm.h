@@ -214,7 +214,11 @@ size_t sgemm_f32_streamk_workspace_size(int M, int N, int K);
  * matrix instructions with the accumulator in tensor memory.  The tiling,
  * pipelining and edge masking are those of the tiled kernel ("Shared Memory
  * Tiling", the tiled kernel and 'What tiling does not fix'), with the inner
- * product on the tensor cores instead of the FP32 cores.
+ * product on the tensor cores instead of the FP32 cores: one persistent
+ * block per SM walks 128-row output tiles (208 columns wide, or 192 down to
+ * 128 when a narrower tile fills the last round of tiles over the SMs better),
+ * with two accumulators so that one tile's stores overlap the next tile's
+ * products.
  *
  * Accuracy: each product carries a relative error of about 3 * 2^-22 from the
  * split, on top of the FP32 accumulation; the result is held to the same bound
@@ -223,10 +227,10 @@ size_t sgemm_f32_streamk_workspace_size(int M, int N, int K);
  * integers are split exactly (A_lo = 0), so integer products whose partial
  * sums stay below 2^24 are exact.
  *
- * A grid of fewer than half as many 128 x 256 output tiles as the device has
- * SMs (e.g. 1024 x 1024 x 1024) has its k-steps divided among up to 16 rows
- * of thread blocks; their partial tiles land in the workspace and are added
- * in row order into C (deterministic, the same bound).
+ * A grid of fewer than half as many 128 x 208 output tiles as the device has
+ * SMs (e.g. 1024 x 1024 x 1024) has its k-steps divided into up to 16 parts;
+ * their partial tiles land in the workspace and are added in part order into
+ * C (deterministic, the same bound).
  *
  * workspace: caller-owned device memory of at least
  * sgemm_f32_3xtf32_workspace_size(M, N, K) bytes, 16-byte aligned, not

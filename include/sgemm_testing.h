@@ -58,6 +58,16 @@ int sgemm_test_switches(int flags, unsigned long long wait_limit_ns);
 int sgemm_f32_plan_model(int M, int N, int K, int path, int sms, long long *tiles, long long *full_tiles,
                          int *cluster_size, int *tile_n);
 
+/*
+ * How sgemm_f32_3xtf32 lays out an M x N x K product on a GPU with `sms`
+ * SMs, without a device: *tile_n = the width of its 128-row output tiles
+ * (256 down to 128 in steps of 16, the width that fills the last round of
+ * tiles over the SMs best) and *splits = the number of CTA rows that divide
+ * the k-steps of a small grid (1: none).  SGEMM_ERR_INVALID_ARG for a NULL
+ * output, a negative size or sms < 1.
+ */
+int sgemm_f32_3xtf32_plan_model(int M, int N, int K, int sms, int *tile_n, int *splits);
+
 #ifdef __cplusplus
 }
 #endif

@@ -155,9 +155,9 @@ def _operand_bytes(M, N, K):
 
 
 def _expected_splits(M, N, K, sms):
-    """The split rule restated: fewer than sms / 2 tiles of 128 x 256 -> up to
+    """The split rule restated: fewer than sms / 2 tiles of 128 x 208 -> up to
     16 rows of blocks, at least eight 16-deep k-steps each, no empty row."""
-    tiles = -(-M // 128) * -(-N // 256)
+    tiles = -(-M // 128) * -(-N // 208)   # the main tile: 128 x 208
     kt = -(-K // 16)
     if 2 * tiles > sms:
         return 1
@@ -175,6 +175,7 @@ def test_divided_products(sg, M, N, K, seed):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     splits = _expected_splits(M, N, K, sms)
     assert splits > 1
+    assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, sms) == (208, splits)
     ldp = (N + 3) // 4 * 4
     assert sg.sgemm_f32_3xtf32_workspace_size(M, N, K) == _operand_bytes(M, N, K) + splits * M * ldp * 4
     A, B = gen.operands(M, N, K, seed=seed)
@@ -223,3 +224,41 @@ def test_divided_product_timeout_reports(sg):
     sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, ws, need)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_full(dC.cpu().numpy(), A, B)
+
+
+# One shape per tile width: 10 rows of tiles (M = 1279, a ragged last row) and
+# N chosen so that the width rule picks each of 208 .. 128 on 152 SMs; K = 40
+# ends in a half k-step.  Each is checked on every element, once with C rows
+# 16-byte aligned (quad stores) and once with ldc = N + 1 (scalar stores).
+WIDTH_SHAPES = {208: 1000, 192: 2641, 176: 2401, 160: 2161, 144: 1921, 128: 1457}
+
+
+@pytest.mark.parametrize("width", sorted(WIDTH_SHAPES))
+@pytest.mark.parametrize("odd_ldc", [False, True])
+def test_every_tile_width(sg, width, odd_ldc):
+    import torch
+    M, N, K = 1279, WIDTH_SHAPES[width], 40
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip(f"widths mapped for 152 SMs, this device has {sms}")
+    assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, sms) == (width, 1)
+    A, B = gen.operands(M, N, K, seed=90 + width)
+    check_full(run_x3(sg, A, B, ldc=N + 1 if odd_ldc else None), A, B)
+
+
+def test_narrow_width_integers_exact_and_alpha_beta(sg):
+    import torch
+    dev = torch.device("cuda", 0)
+    M, N, K = 1279, WIDTH_SHAPES[208], 40
+    Ai = gen.matrix(91, gen.STREAM_A_INT, M, K, "int")
+    Bi = gen.matrix(91, gen.STREAM_B_INT, K, N, "int")
+    check_full(run_x3(sg, Ai, Bi), Ai, Bi, exact=True)
+    # C = 2 A B - 3 C0 on the 3xTF32 algorithm: integers stay exact
+    C0 = gen.matrix(92, gen.STREAM_A_INT, M, N, "int")
+    a, b, c = (torch.from_numpy(x).to(dev) for x in (Ai, Bi, C0))
+    need = sg.sgemm_gemm_workspace_size(1, 0, 0, M, N, K)
+    ws = torch.empty(max(need // 4, 1), device=dev)
+    sg.sgemm_gemm(1, 0, 0, M, N, K, 2.0, a, K, b, N, -3.0, c, N, ws, need)
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    want = 2.0 * (Ai.astype(np.float64) @ Bi.astype(np.float64)) - 3.0 * C0.astype(np.float64)
+    assert np.array_equal(c.cpu().numpy().astype(np.float64), want)
