@@ -47,7 +47,7 @@ import gen  # noqa: E402
 METRIC = "SGEMM TFLOP/s (2MNK/t) and % of FP32 roofline at M=N=K=8192"
 DEFAULT_WORKLOAD = "square_8192"
 # the other workloads, each measured in the line's "configs" block
-CONFIG_WORKLOADS = ["tiny_6x6x9", "square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32"]
+CONFIG_WORKLOADS = ["tiny_6x6x9", "square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32", "square_16384"]
 FLUSH_BYTES = 256 * 2 ** 20   # twice L2: written between steps of workloads that fit in L2
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
@@ -62,8 +62,11 @@ TRAFFIC_PROFILES = {
     "square_8192": ("ffma_tma_square_8192.md", KERNEL_SOURCES, "TmaMainTile"),
     "ragged_3001x4999x2047": ("ffma_phased_ragged_3001x4999x2047.md",
                               ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_phased.cuh"] + KERNEL_SOURCES, "TmaMainTile"),
-    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md", KERNEL_SOURCES, "TmaSmallK1Tile"),
+    "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md",
+                              ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_smallk.cuh"] + KERNEL_SOURCES,
+                              "TmaSmallKStoreTile"),
     "square_1024": ("ffma_narrow_square_1024.md", KERNEL_SOURCES, "TmaNarrowTile"),
+    "square_16384": ("ffma_tma_square_16384.md", KERNEL_SOURCES, "TmaMainTile"),
 }
 
 
@@ -332,9 +335,11 @@ def f32_launches(sg, M, N, K):
 TF32_PEAK_NOTE = ("DERIVED, not measured: dense TF32 tensor peak = {tsrc}; the tensor-core kernel alone "
                   "reads at or above it, so this peak is low and frac overstates the kernel's use of the "
                   "tensor pipe")
-TF32_PROFILES = {"square_8192": "tf32x3_tcgen05_square_8192.md"}
-TF32_SOURCES = ["dense_fp32_matrix_04_gb300/csrc/tf32x3_tcgen05.cuh", "dense_fp32_matrix_04_gb300/csrc/ptx.cuh",
-                "dense_fp32_matrix_04_gb300/csrc/tile_map.cuh"]
+TF32_PROFILES = {"square_8192": "tf32x3_tcgen05_square_8192.md",
+                 "ragged_3001x4999x2047": "tf32x3_tcgen05_ragged_3001x4999x2047.md"}
+TF32_SOURCES = ["dense_fp32_matrix_04_gb300/csrc/tf32x3_tcgen05.cuh", "dense_fp32_matrix_04_gb300/csrc/tcgen05.cuh",
+                "dense_fp32_matrix_04_gb300/csrc/ptx.cuh", "dense_fp32_matrix_04_gb300/csrc/tile_map.cuh",
+                "dense_fp32_matrix_04_gb300/csrc/epilogue.cuh"]
 
 
 def recorded_tensor_pipe(workload):
@@ -376,9 +381,14 @@ def time_steps(step, steps, stream, dev):
 def kernel_name(sg, M, N, K):
     """The kernel sgemm_f32 launches for a contiguous M x K by K x N product."""
     if K > 0 and K % 4 == 0 and N % 4 == 0:
+        if K <= 32:
+            # the bench's products have beta == 0 and a 16-byte aligned C
+            return ("sgemm_ffma_tma_smallk_store_kernel (128x64x32 TMA-fed tile of two warps, 1 stage, 8x16 per "
+                    "thread as fma.rn.f32x2 column pairs with the rows walked down and up in turn; the C tile "
+                    "staged in shared memory and written by TMA bulk tensor stores)")
         if K <= 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed small-K tile, 1 stage, 8x8 per thread as "
-                    f"fma.rn.f32x2 column pairs, k-groups unrolled by {4 if K <= 32 else 8}, 4 CTAs/SM)")
+                    "fma.rn.f32x2 column pairs, k-groups unrolled by 8, 4 CTAs/SM)")
         tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
         if tn == 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed narrow tile, 2 stages, 8x8 per thread as "
@@ -533,6 +543,22 @@ def measure_config(sg, name, dev, stream, sms, props, min_s, flush_buf):
             "roofline": config_roofline(M, N, K, sk_ms, sms, hbm_gbs, hbm_src, sk_clocks),
             "clocks": {k: sk_clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
             "gpu_launches": sk_n, "memsets": sk_n}]
+    if name == "square_16384":
+        # context, not this library: cuBLAS SGEMM (torch.matmul, TF32 off) on the same inputs
+        prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+
+        def cublas_step():
+            torch.matmul(dA, dB, out=dC)
+        for _ in range(2):
+            cublas_step()
+        c_steps, c_ms = timed_steps(cublas_step, stream, dev, None, min(min_s, 1.0))
+        torch.backends.cuda.matmul.allow_tf32 = prev
+        entry["context"] = {"what": "torch.matmul with TF32 off (cuBLAS SGEMM); context only, not this library",
+                            "value": 2.0 * M * N * K / (c_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                            "ms_per_step": c_ms, "steps": c_steps}
+        step()  # the oracle check below reads this library's output
+        torch.cuda.synchronize(dev)
     if name == "tiny_6x6x9":
         entry["us_per_call"] = ms * 1e3
         entry["roofline"]["note"] = "launch-latency bound: 648 FLOP per call"

@@ -17,6 +17,7 @@
 #include "ffma_cp_packed.cuh"
 #include "ffma_tma_phased.cuh"
 #include "ffma_tma_sgemm.cuh"
+#include "ffma_tma_smallk.cuh"
 #include "ffma_tma_streamk.cuh"
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
@@ -485,6 +486,26 @@ int launch_smallk1(const Problem &p, float alpha, float beta, int64_t tiles, cud
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
+// One k-step (K <= 32), beta == 0 and a C the TMA can address (16-byte aligned
+// base and rows, N a multiple of 4): the 8 x 16-per-thread small-K tile whose
+// C tile is written by a TMA store, as a plain grid of 128 x 64 tiles.
+int launch_smallk_store(const Problem &p, float alpha, cudaStream_t stream, const DeviceInfo &info) {
+    using T = sgemm::TmaSmallKStoreTile;
+    using S = sgemm::SmallKStore<T>;
+    alignas(64) CUtensorMap ta, tb, tc;
+    if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tc, p.C, p.M, p.N, p.ldc, T::BM, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SGEMM_ERR_LAUNCH;
+    static std::atomic<int> done[kMaxDevices];
+    if (!smem_attr_once(done[info.dev], sgemm::sgemm_ffma_tma_smallk_store_kernel<T>, S::SMEM_BYTES))
+        return SGEMM_ERR_LAUNCH;
+    const int64_t tiles = (int64_t)((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN);
+    sgemm::sgemm_ffma_tma_smallk_store_kernel<T><<<(unsigned)tiles, T::THREADS, S::SMEM_BYTES, stream>>>(
+        ta, tb, tc, p.M, p.N, p.K, alpha, info.err_word, g_wait_limit_ns.load(), g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
 // Launch the phased TMA kernel (operands whose rows are only 4-byte aligned)
 // over grouped tiles [tile_base, tile_base + tiles), with the same roles as
 // launch_tma.
@@ -612,6 +633,12 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
     if (tma && splits == 1 && p.K <= 2 * TmaSmallK::BK) {
         const int64_t tiles =
             (int64_t)((p.M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((p.N + TmaSmallK::BN - 1) / TmaSmallK::BN);
+        static_assert(sgemm::TmaSmallKStoreTile::BM == TmaSmallK::BM && sgemm::TmaSmallKStoreTile::BN == TmaSmallK::BN,
+                      "one small-K tile shape");
+        // the TMA store writes a row's right edge in 16-byte units: only rows of a
+        // multiple of 4 floats end on a unit boundary (otherwise the store would
+        // also write the gap between N and ldc)
+        if (p.K <= TmaSmallK1::BK && vc && beta == 0.f && p.N % 4 == 0) return launch_smallk_store(p, alpha, stream, info);
         if (p.K <= TmaSmallK1::BK && vc) return launch_smallk1(p, alpha, beta, tiles, stream, info);
         return launch_tma<TmaSmallK>(p, alpha, beta, vc, 1, partials, ldp, 0, tiles, 1, false, stream, info);
     }

@@ -32,6 +32,7 @@
 
 #include "epilogue.cuh"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 #include "tile_map.cuh"
 
 namespace sgemm {

@@ -33,6 +33,16 @@ using TmaSmallKTile = TmaTile<8, 8, 2, 2, 1, 0, 4, 8, true>;
 // at K = 64 the full unroll stays faster (0.615 against 0.636 ms).
 using TmaSmallK1Tile = TmaTile<8, 8, 2, 2, 1, 0, 4, 4, true>;
 
+// Products with a single k-step, beta == 0 and a C the TMA can address, on the
+// kernel that writes C by TMA stores (ffma_tma_smallk.cuh): 128 x 64 tiles of
+// two warps, 8 x 16 packed per thread (the main tile's per-thread work, rows
+// walked down and up in turn), one stage.  Measured at 16384 x 16384 x 32
+// (one product): 0.330 ms against 0.342 ms with per-thread C stores of the
+// same tile, 0.345-0.350 ms for TmaSmallK1Tile, 0.334-0.339 ms for 8 x 16 on
+// 128 x 64 or 64 x 128 tiles without the row walk and 0.435 ms for 128 x 128
+// tiles of four warps at two CTAs per SM.
+using TmaSmallKStoreTile = TmaTile<8, 16, 2, 1, 1, 1, 3, 4, true>;
+
 // Products with fewer 128 x 128 tiles than SMs (e.g. 1024^3, 2048 x 1024 x
 // 2048) on the TMA kernel: 128 x 64 tiles, 8 x 8 packed per thread, 2 stages and 4 blocks per SM
 // (128 registers, no spills), always as thread-block clusters that split each

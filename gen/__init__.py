@@ -132,7 +132,7 @@ def strided(mat: np.ndarray, ld: int, fill: float = np.nan) -> np.ndarray:
     return buf
 
 
-#: The five synthetic workloads of the pages' examples, by name.
+#: The synthetic workloads, by name: the five of the pages' examples and one larger square product.
 #: Each entry: (M, N, K, dist, seed).
 WORKLOADS = {
     "tiny_6x6x9": (6, 6, 9, "uniform", 0),
@@ -140,4 +140,7 @@ WORKLOADS = {
     "square_8192": (8192, 8192, 8192, "normal", 2),
     "ragged_3001x4999x2047": (3001, 4999, 2047, "uniform", 3),
     "skinny_16384x16384x32": (16384, 16384, 32, "uniform", 4),
+    # not one of the pages' examples: the headline's square product at twice
+    # the size, where the FP32 kernel's L2 reuse is tested hardest
+    "square_16384": (16384, 16384, 16384, "normal", 5),
 }

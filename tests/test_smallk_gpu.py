@@ -1,7 +1,8 @@
-"""The small-K tile (K <= 64 on aligned operands: 128 x 64 tiles, one stage,
-four CTAs per SM) on large grids: against the FP64 oracle with ragged edges
-and every K from 1 to 64 class, exactly on small integers, bit for bit against
-the main tile fed by cp.async (the same per-element arithmetic), with
+"""The small-K tiles (K <= 64 on aligned operands: 128 x 64 tiles, one stage;
+for K <= 32 with beta == 0 and a C the TMA can address, the tile whose C is
+written by a TMA store) on large grids: against the FP64 oracle with ragged
+edges and every K from 1 to 64 class, exactly on small integers, bit for bit
+against the main tile fed by cp.async (the same per-element arithmetic), with
 alpha/beta, and on the bounded-wait path with thousands of CTAs."""
 
 import numpy as np
@@ -29,7 +30,7 @@ def ld4(n):
 
 
 @pytest.mark.parametrize("M,N,K", [(2048, 4096, 32), (3001, 2500, 64), (1000, 777 * 4, 1), (4099, 1030, 33),
-                                   (128, 64, 48), (130, 70, 17)])
+                                   (128, 64, 48), (130, 70, 17), (1000, 1030, 32), (257, 100, 32), (5, 36, 3)])
 def test_matches_oracle(sg, M, N, K):
     # leading dimensions padded to 4 floats keep every case on the TMA path
     A, B = gen.operands(M, N, K, seed=300 + K)
@@ -91,3 +92,30 @@ def test_timeout_with_many_ctas(sg, K):
     sg.sgemm_f32(M, N, K, dA, K, dB, N, dC, N)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
     check_rows(dC.cpu().numpy(), A, B, [0, 1000, M - 1])
+
+
+@pytest.mark.parametrize("K", [32, 9])
+def test_tma_store_tile_alpha_bitwise(sg, K):
+    # beta == 0 with a 16-byte aligned C and N a multiple of 4 takes the
+    # TMA-store tile; ldc = N + 1 takes the per-thread stores of the small-K tile: the same accumulators and
+    # alpha * acc rounded once, so the same bits, zero signs included (rows of
+    # zeros in A make products of exactly zero, times a negative alpha)
+    import torch
+    M, N = 1000, 1028
+    A = gen.matrix(315, gen.STREAM_A, M, K)
+    A[::7] = 0.0
+    B = gen.matrix(315, gen.STREAM_B, K, N)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    out = {}
+    for ldc in (N + 4, N + 1):   # N + 4: rows 16-byte aligned (1032); N + 1: not
+        dC = torch.full((M, ldc), float("nan"), device="cuda")
+        sg.sgemm_gemm(0, 0, 0, M, N, K, -1.5, dA, K, dB, N, 0.0, dC, ldc)
+        assert sg.sgemm_device_status() == sg.SGEMM_OK
+        c = dC.cpu().numpy()
+        assert np.isnan(c[:, N:]).all(), "wrote past column N"
+        out[ldc] = c[:, :N].copy()
+    assert np.array_equal(out[N + 4].view(np.int32), out[N + 1].view(np.int32))
+    assert np.signbit(out[N + 4][::7]).all()   # -1.5 * (+0) is -0
+    from oracle import ref_gemm, tolerance
+    C64, S, T = ref_gemm.gemm_general_f64(False, False, -1.5, A, B, 0.0, np.zeros((M, N), np.float32))
+    assert tolerance.max_error_ratio_general(out[N + 4], C64, S, T, K, -1.5) <= 1.0
