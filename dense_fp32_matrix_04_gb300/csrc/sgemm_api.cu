@@ -844,25 +844,27 @@ int x3_splits(int M, int N, int K, int sms, int bn) {
     return (int)((kt + per - 1) / per);
 }
 
-// Tile width of the 3xTF32 product.  With one CTA per SM, a grid of T tiles
-// takes ceil(T / sms) rounds, and a round of 128 x w tiles costs about
-// (w + 128) units: the copies of a k-step move 128 rows of A (hi and lo)
-// whatever the width, and w rows of B.  Fitted to the sweep on GB300 (GEMM
-// alone): against the 208-wide tile, 192 is predicted 1.06x / 1.19x slower at
-// 8192^3 / 3001 x 4999 x 2047 and measured 1.05x / 1.17x; 160 predicted
-// 1.11x / 1.29x, measured 1.12x / 1.29x.  The width with the fewest units
-// wins, ties to the wider tile; grids small enough for the split-K rows keep
-// the main (208-wide) tile.
-int x3_width(int M, int N, int sms) {
+// Tile width of the 3xTF32 product.  With one CTA per SM, a grid of U units
+// (tiles x k-parts) takes ceil(U / sms) rounds, and a round of 128 x w tiles
+// costs about (w + 128) units per k-step: the copies of a k-step move 128 rows
+// of A (hi and lo) whatever the width, and w rows of B.  Fitted to the sweep
+// on GB300 (GEMM alone): against the 208-wide tile, 192 is predicted 1.06x /
+// 1.19x slower at 8192^3 / 3001 x 4999 x 2047 and measured 1.05x / 1.17x;
+// 160 predicted 1.11x / 1.29x, measured 1.12x / 1.29x.  Each width is costed
+// with its own k-parts (x3_splits) as rounds x (w + 128) x the k-steps of a
+// part; the lowest cost wins, ties to the wider tile.
+int x3_width(int M, int N, int K, int sms) {
     using T = X3Tile;
-    if (M <= 0 || N <= 0 || sms <= 0) return T::BN;
+    if (M <= 0 || N <= 0 || K <= 0 || sms <= 0) return T::BN;
     const int64_t tm = (M + T::BM - 1) / T::BM;
-    if (2 * tm * ((N + T::BN - 1) / T::BN) <= sms) return T::BN;
+    const int64_t kt = (K + T::BK - 1) / T::BK;
     int best = T::BN;
     int64_t best_cost = -1;
     for (int bn : sgemm::kTf32x3Widths) {
-        const int64_t rounds = (tm * ((N + bn - 1) / bn) + sms - 1) / sms;
-        const int64_t cost = rounds * (bn + 128);
+        const int s = x3_splits(M, N, K, sms, bn);
+        const int64_t units = tm * ((N + bn - 1) / bn) * s;
+        const int64_t rounds = (units + sms - 1) / sms;
+        const int64_t cost = rounds * (bn + 128) * ((kt + s - 1) / s);
         if (best_cost < 0 || cost < best_cost) best = bn, best_cost = cost;
     }
     return best;
@@ -875,7 +877,7 @@ int64_t up256(int64_t b) { return (b + 255) / 256 * 256; }
 size_t x3_workspace_bytes(int M, int N, int K, int sms) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     const int64_t ops = 4 * x3_kpad(K) * (2 * (int64_t)M + 2 * (int64_t)N);
-    return (size_t)(up256(ops) + (int64_t)partials_bytes(M, N, x3_splits(M, N, K, sms, x3_width(M, N, sms))));
+    return (size_t)(up256(ops) + (int64_t)partials_bytes(M, N, x3_splits(M, N, K, sms, x3_width(M, N, K, sms))));
 }
 
 int device_sms() {
@@ -930,25 +932,28 @@ int launch_3xtf32(const Problem &p, float *ws, cudaStream_t stream, const Device
     float *ah = ws, *al = ws + (int64_t)p.M * kp;
     float *bh = al + (int64_t)p.M * kp, *bl = bh + (int64_t)p.N * kp;
     // A_hi, A_lo are M x K rows and B_hi, B_lo are N x K rows: a row split of an
-    // operand already stored that way, a transposing split otherwise
-    auto split_rows = [&](int rows, const float *src, int ld, float *hi, float *lo) {
-        const dim3 grid((unsigned)(((p.K + 3) / 4 + 255) / 256), (unsigned)(rows < 65535 ? rows : 65535));
-        if (aligned16(src) && ld % 4 == 0)
-            sgemm::split_rows_tf32_kernel<true><<<grid, 256, 0, stream>>>(rows, p.K, src, ld, hi, lo, (int)kp);
-        else
-            sgemm::split_rows_tf32_kernel<false><<<grid, 256, 0, stream>>>(rows, p.K, src, ld, hi, lo, (int)kp);
+    // operand already stored that way, a transposing split otherwise; both in
+    // one launch
+    auto job = [&](int rows, const float *src, int ld, bool transpose, float *hi, float *lo) {
+        sgemm::SplitJob j{src, ld, rows, p.K, hi, lo, (int)kp, transpose ? 1 : 0, 0, 1, 1};
+        if (transpose) {
+            j.gx = (rows + 31) / 32;  // 32 output rows by 32 k per block
+            j.gy = (p.K + 31) / 32;
+        } else {
+            j.vec = aligned16(src) && ld % 4 == 0;
+            j.gx = ((p.K + 3) / 4 + 255) / 256;  // 256 quads of k per block
+            j.gy = rows < 65535 ? rows : 65535;   // rows strided by gy
+        }
+        return j;
     };
-    auto split_transposed = [&](int cols, const float *src, int ld, float *hi, float *lo) {
-        const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((p.K + 31) / 32));
-        sgemm::split_transpose_tf32_kernel<<<grid, 256, 0, stream>>>(p.K, cols, src, ld, hi, lo, (int)kp);
-    };
-    if (p.transa) split_transposed(p.M, p.A, p.lda, ah, al);  // A stored K x M
-    else split_rows(p.M, p.A, p.lda, ah, al);
-    if (p.transb) split_rows(p.N, p.B, p.ldb, bh, bl);        // B stored N x K
-    else split_transposed(p.N, p.B, p.ldb, bh, bl);
+    const sgemm::SplitJob ja = job(p.M, p.A, p.lda, p.transa, ah, al);   // A^T stored K x M: transposing
+    const sgemm::SplitJob jb = job(p.N, p.B, p.ldb, !p.transb, bh, bl);  // B stored K x N: transposing
+    const int64_t blocks = (int64_t)ja.gx * ja.gy + (int64_t)jb.gx * jb.gy;
+    if (blocks > 0x7fffffff) return SGEMM_ERR_INVALID_ARG;
+    sgemm::split_tf32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(ja, jb);
     if (cudaGetLastError() != cudaSuccess) return SGEMM_ERR_LAUNCH;
     float *partials = ws + up256(4 * kp * (2 * (int64_t)p.M + 2 * (int64_t)p.N)) / 4;
-    switch (x3_width(p.M, p.N, info.sms)) {
+    switch (x3_width(p.M, p.N, p.K, info.sms)) {
         case 192: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<192>>(p, ah, al, bh, bl, kp, partials, stream, info);
         case 176: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<176>>(p, ah, al, bh, bl, kp, partials, stream, info);
         case 160: return launch_3xtf32_gemm<sgemm::Tf32x3WidthTile<160>>(p, ah, al, bh, bl, kp, partials, stream, info);
@@ -1060,7 +1065,7 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
 
 int sgemm_f32_3xtf32_plan_model(int M, int N, int K, int sms, int *tile_n, int *splits) {
     if (!tile_n || !splits || M < 0 || N < 0 || K < 0 || sms < 1) return SGEMM_ERR_INVALID_ARG;
-    *tile_n = x3_width(M, N, sms);
+    *tile_n = x3_width(M, N, K, sms);
     *splits = x3_splits(M, N, K, sms, *tile_n);
     return SGEMM_OK;
 }

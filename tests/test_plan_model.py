@@ -129,3 +129,52 @@ def test_model_rejects_bad_arguments(args):
     st = sg.load().sgemm_f32_plan_model(M, N, K, path, sms, ctypes.byref(t), ctypes.byref(f), ctypes.byref(c),
                                         ctypes.byref(n))
     assert st == sg.SGEMM_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- 3xTF32 layout
+
+def x3_expected_splits(M, N, K, sms, width):
+    """The 3xTF32 split rule restated: fewer than sms / 2 tiles of 128 x width
+    -> up to 16 k-parts, at least eight 16-deep k-steps each, no empty part."""
+    tiles = -(-M // 128) * -(-N // width)
+    kt = -(-K // 16)
+    if 2 * tiles > sms:
+        return 1
+    s = min(sms // tiles, kt // 8, 16)
+    if s < 2:
+        return 1
+    per = -(-kt // s)
+    return -(-kt // per)
+
+
+def x3_expected_layout(M, N, K, sms):
+    """The 3xTF32 width rule restated: each width w in 208, 192, ..., 128 with
+    its own k-parts s costs ceil(tiles * s / sms) rounds x (w + 128) x
+    ceil(kt / s); the cheapest wins, ties to the wider tile."""
+    kt = -(-K // 16)
+    best = None
+    for w in (208, 192, 176, 160, 144, 128):
+        s = x3_expected_splits(M, N, K, sms, w)
+        cost = -(-(-(-M // 128) * -(-N // w) * s) // sms) * (w + 128) * -(-kt // s)
+        if best is None or cost < best[0]:
+            best = (cost, w, s)
+    return best[1], best[2]
+
+
+def test_3xtf32_layout_follows_the_rule():
+    import random
+    rng = random.Random(7)
+    for _ in range(2000):
+        M, N, K = rng.randint(1, 9000), rng.randint(1, 9000), rng.randint(1, 20000)
+        sms = rng.choice([148, 152, 160])
+        assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, sms) == x3_expected_layout(M, N, K, sms), (M, N, K, sms)
+
+
+@pytest.mark.parametrize("M,N,K,want", [
+    # measured fastest on GB300 (GEMM alone, 340.7 and 300.9 TFLOP/s against 333.3 and 246.4
+    # for 128 x 256 with four stages): 128 x 208 with five stages
+    (8192, 8192, 8192, (208, 1)), (3001, 4999, 2047, (208, 1)),
+    # 600 tiles of 208 fill 3.95 rounds; 1024^3: 48 tiles of 176 x 3 k-parts fill 144 of 152 SMs
+    (1024, 1024, 1024, (176, 3))])
+def test_3xtf32_layout_on_the_workloads(M, N, K, want):
+    assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, SMS) == want

@@ -154,18 +154,7 @@ def _operand_bytes(M, N, K):
     return (4 * kpad * (2 * M + 2 * N) + 255) // 256 * 256
 
 
-def _expected_splits(M, N, K, sms):
-    """The split rule restated: fewer than sms / 2 tiles of 128 x 208 -> up to
-    16 rows of blocks, at least eight 16-deep k-steps each, no empty row."""
-    tiles = -(-M // 128) * -(-N // 208)   # the main tile: 128 x 208
-    kt = -(-K // 16)
-    if 2 * tiles > sms:
-        return 1
-    s = min(sms // tiles, kt // 8, 16)
-    if s < 2:
-        return 1
-    per = -(-kt // s)
-    return -(-kt // per)
+from test_plan_model import x3_expected_layout as _expected_layout  # noqa: E402
 
 
 @pytest.mark.parametrize("M,N,K,seed", [(256, 256, 4096, 80), (1024, 1024, 1024, 81), (300, 200, 1000, 82),
@@ -173,9 +162,9 @@ def _expected_splits(M, N, K, sms):
 def test_divided_products(sg, M, N, K, seed):
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    splits = _expected_splits(M, N, K, sms)
+    width, splits = _expected_layout(M, N, K, sms)
     assert splits > 1
-    assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, sms) == (208, splits)
+    assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, sms) == (width, splits)
     ldp = (N + 3) // 4 * 4
     assert sg.sgemm_f32_3xtf32_workspace_size(M, N, K) == _operand_bytes(M, N, K) + splits * M * ldp * 4
     A, B = gen.operands(M, N, K, seed=seed)
@@ -230,7 +219,7 @@ def test_divided_product_timeout_reports(sg):
 # N chosen so that the width rule picks each of 208 .. 128 on 152 SMs; K = 40
 # ends in a half k-step.  Each is checked on every element, once with C rows
 # 16-byte aligned (quad stores) and once with ldc = N + 1 (scalar stores).
-WIDTH_SHAPES = {208: 1000, 192: 2641, 176: 2401, 160: 2161, 144: 1921, 128: 1457}
+WIDTH_SHAPES = {208: 2881, 192: 2641, 176: 2401, 160: 2161, 144: 1921, 128: 1000}
 
 
 @pytest.mark.parametrize("width", sorted(WIDTH_SHAPES))
