@@ -21,6 +21,7 @@
 #include "ffma_tma_streamk.cuh"
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
+#include "tf32_split.cuh"
 #include "tf32x3_tcgen05.cuh"
 #include "tiles.cuh"
 
