@@ -48,6 +48,8 @@ METRIC = "SGEMM TFLOP/s (2MNK/t) and % of FP32 roofline at M=N=K=8192"
 DEFAULT_WORKLOAD = "square_8192"
 # the other workloads, each measured in the line's "configs" block
 CONFIG_WORKLOADS = ["tiny_6x6x9", "square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32", "square_16384"]
+# configs also timed through sgemm_f32_3xtf32 (the headline's variant is timed beside the headline)
+X3_CONFIG_WORKLOADS = ["square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32"]
 FLUSH_BYTES = 256 * 2 ** 20   # twice L2: written between steps of workloads that fit in L2
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
@@ -543,6 +545,36 @@ def measure_config(sg, name, dev, stream, sms, props, min_s, flush_buf):
             "roofline": config_roofline(M, N, K, sk_ms, sms, hbm_gbs, hbm_src, sk_clocks),
             "clocks": {k: sk_clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
             "gpu_launches": sk_n, "memsets": sk_n}]
+    if name in X3_CONFIG_WORKLOADS:
+        # the same product on the tensor cores (sgemm_f32_3xtf32, caller workspace allocated untimed)
+        x3_bytes = sg.sgemm_f32_3xtf32_workspace_size(M, N, K)
+        x3_ws = torch.empty(max(x3_bytes // 4, 4), dtype=torch.float32, device=dev)
+
+        def x3_step():
+            sg.sgemm_f32_3xtf32(M, N, K, dA, K, dB, N, dC, N, x3_ws, x3_bytes, handle)
+        for _ in range(3):
+            x3_step()
+        sampler = ClockSampler(str(getattr(props, "uuid", "")))
+        sampler.start()
+        x3_n, x3_ms = timed_steps(x3_step, stream, dev, flush, min_s)
+        x3_clocks = sampler.stop()
+        tpk, tsrc = tf32_peak_tflops()
+        x3_tf = 2.0 * M * N * K / (x3_ms / 1e3) / 1e12
+        width, parts = sg.sgemm_f32_3xtf32_plan_model(M, N, K, sms)
+        entry.setdefault("variants", []).append({
+            "path": f"sgemm_f32_3xtf32 (tensor cores, 3xTF32 split precision; 128x{width} tiles"
+                    + (f", {parts} k-parts" if parts > 1 else "") + ")",
+            "steps": x3_n, "ms_per_step": x3_ms, "value": x3_tf, "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": 3 * x3_tf, "peak": tpk, "unit": "TFLOP/s",
+                         "frac": 3 * x3_tf / tpk, "peak_basis": TF32_PEAK_NOTE.format(tsrc=tsrc),
+                         "tensor_pipe_active_ncu": recorded_tensor_pipe(name),
+                         "note": "3 TF32 products per FP32 product over the whole step (operand splitting "
+                                 "included); tensor_pipe_active_ncu is the hardware counter's fraction"},
+            "clocks": {k: x3_clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+            "gpu_launches": 2 * x3_n + (x3_n if parts > 1 else 0)})
+        step()  # the oracle check below reads sgemm_f32's output
+        torch.cuda.synchronize(dev)
+        del x3_ws
     if name == "square_16384":
         # context, not this library: cuBLAS SGEMM (torch.matmul, TF32 off) on the same inputs
         prev = torch.backends.cuda.matmul.allow_tf32
