@@ -382,6 +382,9 @@ def time_steps(step, steps, stream, dev):
 
 def kernel_name(sg, M, N, K):
     """The kernel sgemm_f32 launches for a contiguous M x K by K x N product."""
+    if K > 0 and sg.sgemm_f32_plan(M, N, K)[3] == 0:
+        return ("sgemm_ffma_tiny_kernel (one thread per output, the K-long dot product read straight from "
+                "memory; products of at most 16384 outputs with K <= 128)")
     if K > 0 and K % 4 == 0 and N % 4 == 0:
         if K <= 32:
             # the bench's products have beta == 0 and a 16-byte aligned C

@@ -89,6 +89,7 @@ _SIGNATURES = {
     "sgemm_device_status": (ctypes.c_int, [ctypes.c_void_p]),
     # test-only interface (include/sgemm_testing.h)
     "sgemm_test_switches": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
+    "sgemm_test_tiny_path": (ctypes.c_int, [ctypes.c_int]),
     "sgemm_f32_plan_model": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                             ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_longlong),
                                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
@@ -334,6 +335,12 @@ def sgemm_test_switches(flags: int, wait_limit_ns: int = 2_000_000_000) -> None:
 
 
 PLAN_PATHS = {"tma": 0, "phased": 1, "cp": 2}
+
+
+def sgemm_test_tiny_path(enable: bool) -> None:
+    """Test-only: tiny products take the one-thread-per-output kernel (True,
+    the default) or the tiled kernels (False); needs SGEMM_TEST_SWITCHES=1."""
+    _check(load().sgemm_test_tiny_path(1 if enable else 0), "sgemm_test_tiny_path")
 
 
 def sgemm_f32_plan_model(M: int, N: int, K: int, sms: int, path: str = "tma"):

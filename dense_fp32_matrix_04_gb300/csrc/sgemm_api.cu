@@ -19,6 +19,7 @@
 #include "ffma_tma_sgemm.cuh"
 #include "ffma_tma_smallk.cuh"
 #include "ffma_tma_streamk.cuh"
+#include "ffma_tiny.cuh"
 #include "ladder.cuh"
 #include "splitk_reduce.cuh"
 #include "tf32_split.cuh"
@@ -67,6 +68,8 @@ constexpr int kDebugForcePhased = 2048;
 constexpr int kDebugForceStreamK = 4096;  // sgemm_f32_streamk: stream-K whatever the tile count
 constexpr int kDebugStreamKPerSmShift = 13;  // bits 13..14: stream-K blocks per SM (0 = one)
 std::atomic<int> g_debug_flags{0};
+// test-only (sgemm_test_tiny_path): tiny products take the one-thread-per-output kernel
+std::atomic<int> g_tiny_path{1};
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
 struct DeviceInfo {
@@ -615,11 +618,29 @@ int launch_cp(const Problem &p, float alpha, float beta, bool vc, int splits, fl
 // 4-byte aligned (M, K >= 4), otherwise on the cp.async-fed kernel.  splits > 1
 // writes partial sums to `partials` (splits slabs of M x ldp) instead of C;
 // splits == 1 follows the cluster-split plan.
+// Products for which one thread per output beats the tiled kernels' set-up:
+// at most kTinyOutputs outputs with at most kTinyK terms each.  Measured on
+// GB300 (µs per call, one thread per output against the tiled plan): 6x6x9
+// 3.7-4.1 against 6.6; 32x32x64 6.1 against 7.2 (10.3 with odd strides);
+// 128x128x128 9.7 against 16.4; 256x128x128 10.2 against 16.4; at K = 256
+// the two are even (14.3-16.4) and at K = 512 the tiled plan is twice as fast.
+constexpr int kTinyOutputs = 16384;
+constexpr int kTinyK = 128;
+bool tiny_product(const Problem &p) {
+    return (int64_t)p.M * p.N <= kTinyOutputs && p.K <= kTinyK && p.K > 0 && g_tiny_path.load();
+}
+
 int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaStream_t stream,
                    const DeviceInfo &info) {
     const bool vc = splits > 1 || (aligned16(p.C) && p.ldc % 4 == 0);
     // partial slabs hold the raw products; alpha and beta act in the reduction
     const float alpha = splits > 1 ? 1.f : p.alpha, beta = splits > 1 ? 0.f : p.beta;
+    if (splits == 1 && tiny_product(p)) {
+        sgemm::sgemm_ffma_tiny_kernel<<<(unsigned)((p.M * p.N + sgemm::kTinyThreads - 1) / sgemm::kTinyThreads),
+                                        sgemm::kTinyThreads, 0, stream>>>(p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C,
+                                                                           p.ldc, alpha, beta);
+        return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    }
     const bool tma = use_tma(p);
     const bool phased = !tma && use_phased(p);
     if (!tma && !phased && !cp_fits(p)) {
@@ -1053,6 +1074,14 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
     const int dbg = g_debug_flags.load();
     const bool cp = !tma_operands || (dbg & (kDebugForceCpAsync | kDebugForcePhased)) != 0;
     const bool phased = cp && M >= 4 && K >= 4 && !(dbg & kDebugForceCpAsync);
+    if (M >= 0 && N >= 0 && K > 0 && (int64_t)M * N > 0 && (int64_t)M * N <= kTinyOutputs && K <= kTinyK &&
+        g_tiny_path.load() && tiles && full_tiles && cluster_size && tile_n) {
+        // one thread per output, in blocks of 256
+        *tiles = *full_tiles = ((long long)M * N + sgemm::kTinyThreads - 1) / sgemm::kTinyThreads;
+        *cluster_size = 1;
+        *tile_n = 0;
+        return SGEMM_OK;
+    }
     auto on_device = [&](Narrow narrow, bool ph, int &st) {
         DeviceInfo info;
         if (device_info(info) != SGEMM_OK) {
@@ -1573,6 +1602,13 @@ int sgemm_device_status(cudaStream_t stream) {
             return SGEMM_ERR_DEVICE;
         return SGEMM_ERR_TIMEOUT;
     }
+    return SGEMM_OK;
+}
+
+int sgemm_test_tiny_path(int enable) {
+    const char *on = std::getenv("SGEMM_TEST_SWITCHES");
+    if (!on || std::strcmp(on, "1") != 0 || (enable != 0 && enable != 1)) return SGEMM_ERR_INVALID_ARG;
+    g_tiny_path.store(enable);
     return SGEMM_OK;
 }
 

@@ -96,7 +96,10 @@ typedef enum {
  * thread; four blocks per SM on the TMA and phased paths, three on the
  * cp.async path, the latter only when 16 * lda and 8 * ldb fit in 32 bits),
  * all in such clusters
- * (sgemm_f32_plan reports the choice).
+ * (sgemm_f32_plan reports the choice).  Tiny products -- at most 16384
+ * outputs, 1 <= K <= 128, on any path -- skip the tiles: one thread per output
+ * computes its dot product straight from memory (the pages' naive kernel),
+ * which for them costs a fraction of the tiled kernels' set-up.
  * Returns an sgemm_status.  M == 0 or N == 0: SGEMM_OK, nothing launched.
  * The TMA kernels' waits are bounded: if a copy never lands, its blocks give
  * up, write nothing, and the next sgemm_device_status() returns
@@ -122,7 +125,10 @@ int sgemm_f32(int M, int N, int K,
  * phased TMA kernel's plan; smaller ones the cp.async kernel's, which assumes
  * 16 * lda and 8 * ldb fit in 32 bits (otherwise the 128 x 128 plan runs).  The result
  * reflects the switches of the test-only interface (sgemm_testing.h), which
- * are all off unless a test turned them on.  Launches nothing.
+ * are all off unless a test turned them on.  Tiny products (at most 16384
+ * outputs, 1 <= K <= 128) report *tile_n = 0, *cluster_size = 1 and
+ * *tiles = *full_tiles = the blocks of 256 outputs of the one-thread-per-output
+ * kernel.  Launches nothing.
  * SGEMM_ERR_INVALID_ARG for a NULL output or negative size; SGEMM_ERR_DEVICE
  * if the device cannot be queried.
  */

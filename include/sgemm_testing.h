@@ -42,6 +42,18 @@ extern "C" {
 int sgemm_test_switches(int flags, unsigned long long wait_limit_ns);
 
 /*
+ * Turns the one-thread-per-output kernel that sgemm_f32 uses for tiny
+ * products (at most 16384 outputs, 1 <= K <= 128) on (enable = 1, the default)
+ * or off (0: they take the tiled kernels like larger products), for every
+ * later product in this process.  The library's tests turn it off so that
+ * their small shapes reach the tiled kernels' edge handling, and on where
+ * they test the tiny kernel itself.  Same environment condition as
+ * sgemm_test_switches; SGEMM_ERR_INVALID_ARG otherwise or if enable is not 0
+ * or 1.
+ */
+int sgemm_test_tiny_path(int enable);
+
+/*
  * The planner of sgemm_f32 without a device: the plan sgemm_f32_plan reports
  * (same outputs, same meaning) for the kernel path `path` -- 0: operands the
  * TMA can address (the TMA kernel, its small-K tile for 1 <= K <= 64);
