@@ -1,5 +1,26 @@
 // The C interface of libsgemm: argument checks, kernel choice and launch.
-// Declarations and the full contract are in include/sgemm.h.
+// Declarations and the full contract are in include/sgemm.h (and the
+// test-only entry points in include/sgemm_testing.h).
+//
+// How sgemm_f32 chooses a kernel (launch_product), in order:
+//   1. tiny products (<= 16384 outputs, K <= 128): one thread per output
+//      (ffma_tiny.cuh);
+//   2. operands the TMA can address (16-byte aligned bases and rows):
+//      K <= 32 with beta == 0 and N % 4 == 0 -> the TMA-store small-K tile
+//      (ffma_tma_smallk.cuh); K <= 64 -> the 8 x 8 small-K tile; otherwise the
+//      main 128 x 128 tile (ffma_tma_sgemm.cuh), planned by split_plan;
+//   3. rows only 4-byte aligned, M >= 4 and K >= 4: the same tiles read through
+//      four phase maps per operand (ffma_tma_phased.cuh), planned likewise;
+//   4. otherwise the cp.async-fed kernel (ffma_cp_packed.cuh), or for A rows
+//      more than 2 GiB apart the pages' register-tiled ladder kernel.
+// split_plan (the fitted cost models; split_plan_model is the device-free
+// part) decides between a plain grid, a plain grid plus the cluster split of
+// its last partial round of tiles, and narrow 128 x 64 tiles in clusters.
+// The other entry points reuse these launches: split-K and its allocation-free
+// form (partials + splitk_reduce.cuh), stream-K (ffma_tma_streamk.cuh), the
+// 3xTF32 product (tf32_split.cuh + tf32x3_tcgen05.cuh, x3_width choosing the
+// tile width), sgemm_gemm (repacks transposed or unaligned operands when the
+// FFMA path needs it) and the host-buffer pipeline at the end of the file.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
