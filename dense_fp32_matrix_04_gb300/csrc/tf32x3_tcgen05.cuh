@@ -235,8 +235,12 @@ __global__ void __launch_bounds__(T::THREADS, 1)
             int m0, n0, kt0, kts;
             unit(u, m0, n0, kt0, kts);
             const int b = i & 1;
+            // a finished accumulator is stored whatever another role decided
+            // since, so every drain warp stores all of a tile or none of it
+            // (the MMA thread commits no tile after giving up, and then every
+            // drain warp's wait runs out)
             const bool ready = mbar_wait_bounded(acc_full0 + 8 * b, (i >> 1) & 1, wait_limit_ns);
-            if (!__all_sync(0xffffffffu, ready && !*abort_flag)) {
+            if (!__all_sync(0xffffffffu, ready)) {
                 if (lane == 0) *abort_flag = 1;
                 break;
             }
