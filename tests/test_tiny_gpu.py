@@ -90,3 +90,34 @@ def test_alpha_beta(sg):
     C64, S, T = ref_gemm.gemm_general_f64(False, False, 1.75, A, B, -0.5, C0)
     assert tolerance.max_error_ratio_general(out[True], C64, S, T, K, 1.75) <= 1.0
     assert np.array_equal(out[True].view(np.int32), out[False].view(np.int32))
+
+
+@pytest.mark.parametrize("M,N,K", [(6, 6, 9), (100, 163, 77)])
+def test_other_entry_points_on_tiny_products(sg, M, N, K):
+    # every entry point that runs sgemm_f32's launch takes the same kernel for
+    # tiny products: one split of split-K, stream-K (which falls back to
+    # sgemm_f32 when its plan fills the SMs), the allocation-free split-K and
+    # the host-buffer pipeline; each result equals sgemm_f32's bit for bit
+    import torch
+    A, B = gen.operands(M, N, K, seed=614)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    want = sg.matmul(dA, dB)
+    got = {}
+    got["splitk"] = sg.matmul_splitk(dA, dB, splits=1)
+    got["streamk"] = sg.matmul_streamk(dA, dB)
+    c = torch.empty_like(want)
+    sg.sgemm_f32_splitk_noalloc(M, N, K, dA, K, dB, N, c, N, 1)
+    got["noalloc"] = c
+    hA, hB = torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    ws_bytes = sg.sgemm_f32_host_workspace_size(M, N, K, 1)
+    ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device="cuda")
+    s0, s1, s2 = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    sg.sgemm_f32_host(M, N, K, hA, K, hB, N, hC, N, 1, ws, ws_bytes, s0, s1, s2)
+    s0.synchronize()
+    torch.cuda.synchronize()
+    got["host"] = hC.cuda()
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+    for name, c in got.items():
+        assert torch.equal(c, want), name
+    check_full(want.cpu().numpy(), A, B)
