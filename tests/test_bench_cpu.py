@@ -53,7 +53,10 @@ def test_recorded_traffic_follows_the_kernel_sources():
     # still sit in L2 when the launch ends, so only the operand reads bound it
     r = bench.recorded_traffic("ragged_3001x4999x2047")
     assert r is None or r > 4 * (3001 * 2047 + 2047 * 4999)
-    assert bench.recorded_traffic("tiny_6x6x9") is None
+    # 6x6x9 moves 576 algorithmic bytes; its capture reads a few kB (a cold launch)
+    t0 = bench.recorded_traffic("tiny_6x6x9")
+    assert t0 is None or t0 < 1_000_000
+    assert bench.recorded_traffic("no_such_workload") is None
     assert len(bench.kernel_source_digest()) == 16
     for name, sources, tile in bench.TRAFFIC_PROFILES.values():
         assert os.path.exists(os.path.join(bench.ROOT, "profiles", name))
