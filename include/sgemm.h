@@ -68,7 +68,10 @@ typedef enum {
  *   - A and B with 16-byte aligned bases and leading dimensions (multiples of
  *     4 floats), K >= 1: 128 x 128 block tiles copied by the tensor memory
  *     accelerator (TMA) with hardware zero-fill at the edges, 8 x 16 outputs
- *     per thread accumulated with packed two-wide FP32 FMAs;
+ *     per thread accumulated with packed two-wide FP32 FMAs; K <= 64 takes
+ *     128 x 64 tiles of a single stage, and a single k-step (K <= 32) with a
+ *     16-byte aligned C whose row length N is a multiple of 4 writes its C
+ *     tiles by TMA stores from shared memory;
  *   - otherwise, with M >= 4 and K >= 4: the same tiles and packed FMAs, each
  *     operand read by the TMA through four tensor maps, one per residue of
  *     the row index mod 4 (those rows are 4 * ld floats apart, a multiple of
