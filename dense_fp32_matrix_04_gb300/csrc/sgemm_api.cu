@@ -1070,6 +1070,12 @@ int report_plan(int M, int N, int K, int path, PlanFn plan_fn, long long *tiles,
     *cluster_size = 1;
     *tile_n = TmaTile::BN;
     if ((int64_t)M * N == 0) return SGEMM_OK;
+    if (tiny_product(Problem{M, N, K, nullptr, 1, nullptr, 1, nullptr, 1})) {
+        // one thread per output, in blocks of 256
+        *tiles = *full_tiles = ((long long)M * N + sgemm::kTinyThreads - 1) / sgemm::kTinyThreads;
+        *tile_n = 0;
+        return SGEMM_OK;
+    }
     if (K <= 2 * TmaSmallK::BK && K > 0 && path == 0) {
         *tiles = *full_tiles =
             (long long)((M + TmaSmallK::BM - 1) / TmaSmallK::BM) * ((N + TmaSmallK::BN - 1) / TmaSmallK::BN);
@@ -1095,14 +1101,6 @@ int sgemm_f32_plan(int M, int N, int K, int tma_operands, long long *tiles, long
     const int dbg = g_debug_flags.load();
     const bool cp = !tma_operands || (dbg & (kDebugForceCpAsync | kDebugForcePhased)) != 0;
     const bool phased = cp && M >= 4 && K >= 4 && !(dbg & kDebugForceCpAsync);
-    if (M >= 0 && N >= 0 && K > 0 && (int64_t)M * N > 0 && (int64_t)M * N <= kTinyOutputs && K <= kTinyK &&
-        g_tiny_path.load() && tiles && full_tiles && cluster_size && tile_n) {
-        // one thread per output, in blocks of 256
-        *tiles = *full_tiles = ((long long)M * N + sgemm::kTinyThreads - 1) / sgemm::kTinyThreads;
-        *cluster_size = 1;
-        *tile_n = 0;
-        return SGEMM_OK;
-    }
     auto on_device = [&](Narrow narrow, bool ph, int &st) {
         DeviceInfo info;
         if (device_info(info) != SGEMM_OK) {

@@ -61,7 +61,8 @@ int sgemm_test_tiny_path(int enable);
  * (sgemm_f32 takes it when M >= 4 and K >= 4); 2: the cp.async-fed kernel
  * (which sgemm_f32 takes for the remaining unaligned products) -- computed
  * for a GPU with `sms` SMs on which clusters of 2, 4 and 8 blocks can all be
- * resident, with every test switch off.  It lets the cost models that choose
+ * resident, with every test switch off (the tiny-product path follows
+ * sgemm_test_tiny_path).  It lets the cost models that choose
  * between the plain grid, the cluster split and the narrow tile be checked
  * on a machine without a GPU.  Launches nothing and makes no CUDA call.
  * SGEMM_ERR_INVALID_ARG for a NULL output, a negative size, sms < 1 or an

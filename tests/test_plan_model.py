@@ -114,6 +114,20 @@ def test_small_k_tile_for_tma_operands_only():
     assert sg.sgemm_f32_plan_model(16384, 16384, 32, SMS, "phased") == (16384, 16384, 1, 128)
 
 
+def test_tiny_products_skip_the_tiles():
+    # at most 16384 outputs with 1 <= K <= 128: one thread per output, on every path
+    for path in ("tma", "phased", "cp"):
+        assert sg.sgemm_f32_plan_model(6, 6, 9, SMS, path) == (1, 1, 1, 0)
+        assert sg.sgemm_f32_plan_model(128, 128, 128, SMS, path) == (64, 64, 1, 0)
+        assert sg.sgemm_f32_plan_model(128, 128, 129, SMS, path)[3] != 0
+        assert sg.sgemm_f32_plan_model(128, 129, 128, SMS, path)[3] != 0
+    sg.sgemm_test_tiny_path(False)
+    try:
+        assert sg.sgemm_f32_plan_model(6, 6, 9, SMS, "tma")[3] == 64   # the small-K tile
+    finally:
+        sg.sgemm_test_tiny_path(True)
+
+
 def test_the_plan_follows_the_sm_count():
     # one full round on 152 SMs is a partial one on 148
     assert sg.sgemm_f32_plan_model(2432, 1024, 4096, SMS, "tma") == (152, 152, 1, 128)
