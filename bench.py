@@ -47,7 +47,8 @@ import gen  # noqa: E402
 METRIC = "SGEMM TFLOP/s (2MNK/t) and % of FP32 roofline at M=N=K=8192"
 DEFAULT_WORKLOAD = "square_8192"
 # the other workloads, each measured in the line's "configs" block
-CONFIG_WORKLOADS = ["tiny_6x6x9", "square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32", "square_16384"]
+CONFIG_WORKLOADS = ["tiny_6x6x9", "square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32", "square_16384",
+                    "longk_256x256x65536"]
 # configs also timed through sgemm_f32_3xtf32 (the headline's variant is timed beside the headline)
 X3_CONFIG_WORKLOADS = ["square_1024", "ragged_3001x4999x2047", "skinny_16384x16384x32"]
 FLUSH_BYTES = 256 * 2 ** 20   # twice L2: written between steps of workloads that fit in L2
@@ -72,6 +73,11 @@ TRAFFIC_PROFILES = {
     "tiny_6x6x9": ("ffma_tiny_6x6x9.md", ["dense_fp32_matrix_04_gb300/csrc/ffma_tiny.cuh",
                                           "dense_fp32_matrix_04_gb300/csrc/epilogue.cuh"], None),
 }
+# the same for sgemm_f32_streamk's kernel, on the workloads that take it
+STREAMK_PROFILES = {
+    "longk_256x256x65536": ("ffma_tma_streamk_longk_256x256x65536.md",
+                            ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_streamk.cuh"] + KERNEL_SOURCES, "TmaMainTile"),
+}
 
 
 def log(*a):
@@ -89,9 +95,11 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=10)
-    p.add_argument("--path", choices=["ffma", "splitk", "3xtf32", "gemm"] + sorted(LADDER), default="ffma",
+    p.add_argument("--path", choices=["ffma", "splitk", "streamk", "3xtf32", "gemm"] + sorted(LADDER),
+                   default="ffma",
                    help="ffma: sgemm_f32 (the headline); splitk: sgemm_f32_splitk with the suggested split "
-                        "count; 3xtf32: sgemm_f32_3xtf32 (tensor cores). Workspaces are allocated untimed.")
+                        "count; streamk: sgemm_f32_streamk; 3xtf32: sgemm_f32_3xtf32 (tensor cores). "
+                        "Workspaces are allocated untimed.")
     p.add_argument("--no-context", action="store_true",
                    help="skip the torch.matmul (cuBLAS SGEMM) context timing")
     p.add_argument("--no-variants", action="store_true",
@@ -253,12 +261,14 @@ def kernel_source_digest(sources=None, tile=None):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload=DEFAULT_WORKLOAD):
-    """DRAM bytes of one product of the workload from its committed ncu summary,
-    if the capture was taken on the kernel sources as they are now; else None."""
-    if workload not in TRAFFIC_PROFILES:
+def recorded_traffic(workload=DEFAULT_WORKLOAD, profiles=None):
+    """DRAM bytes of one product of the workload from its committed ncu summary
+    (sgemm_f32's kernel, or the kernel of the table ``profiles``), if the
+    capture was taken on the kernel sources as they are now; else None."""
+    profiles = TRAFFIC_PROFILES if profiles is None else profiles
+    if workload not in profiles:
         return None
-    name, sources, tile = TRAFFIC_PROFILES[workload]
+    name, sources, tile = profiles[workload]
     try:
         text = open(os.path.join(ROOT, "profiles", name)).read()
     except OSError:
@@ -299,6 +309,15 @@ def make_step(sg, path, M, N, K, dA, dB, dC, handle, cfg, dev):
         # the same launches as sgemm_f32 (a repacking copy, below four rows, is
         # not a kernel of ours)
         return step, f32_launches(sg, M, N, K)
+    if path == "streamk":
+        ws_bytes = sg.sgemm_f32_streamk_workspace_size(M, N, K)
+        ws = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+        cfg["path"] = "sgemm_f32_streamk" + ("" if ws_bytes else " (runs as sgemm_f32: its plan fills the SMs)")
+
+        def step():
+            sg.sgemm_f32_streamk(M, N, K, dA, K, dB, N, dC, N, ws, ws_bytes, handle)
+        # one kernel (and a memset of the tile counters) when stream-K is taken
+        return step, (1 if ws_bytes else f32_launches(sg, M, N, K))
     if path in LADDER:
         cfg["path"] = path
 
@@ -380,6 +399,12 @@ def time_steps(step, steps, stream, dev):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     return e0.elapsed_time(e1)
+
+
+STREAMK_KERNEL = ("sgemm_ffma_tma_streamk_kernel (128x128x32 TMA-fed tile, 3 stages, 8x16 per thread as "
+                  "fma.rn.f32x2 column pairs; a cooperative grid of two blocks per SM, each an equal run of (tile, "
+                  "k-step) units across tile boundaries; partial tiles meet in the caller's workspace and every "
+                  "block that shares a tile adds up its own slice of them in a fixed order)")
 
 
 def kernel_name(sg, M, N, K):
@@ -543,11 +568,14 @@ def measure_config(sg, name, dev, stream, sms, props, min_s, flush_buf):
         sampler.start()
         sk_n, sk_ms = timed_steps(sk_step, stream, dev, flush, min_s)
         sk_clocks = sampler.stop()
+        sk_roof = config_roofline(M, N, K, sk_ms, sms, hbm_gbs, hbm_src, sk_clocks)
+        sk_roof["traffic"] = recorded_traffic(name, STREAMK_PROFILES)
         entry["variants"] = [{
             "path": "sgemm_f32_streamk (equal runs of (tile, k-step) units per resident block; caller workspace "
                     f"of {sk_bytes / 2 ** 20:.1f} MiB, allocated untimed)",
+            "kernel": STREAMK_KERNEL,
             "steps": sk_n, "ms_per_step": sk_ms, "value": 2.0 * M * N * K / (sk_ms / 1e3) / 1e12, "unit": "TFLOP/s",
-            "roofline": config_roofline(M, N, K, sk_ms, sms, hbm_gbs, hbm_src, sk_clocks),
+            "roofline": sk_roof,
             "clocks": {k: sk_clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
             "gpu_launches": sk_n, "memsets": sk_n}]
     if name in X3_CONFIG_WORKLOADS:
@@ -788,6 +816,9 @@ def run_ours(args):
                                                  if cfg.get("splitk", 1) > 1 else "")
     if args.path in LADDER:
         roofline["kernel"] = f"{args.path} (the pages' kernel ladder)"
+    if args.path == "streamk" and sg.sgemm_f32_streamk_workspace_size(M, N, K) > 0:
+        roofline["kernel"] = STREAMK_KERNEL
+        roofline["traffic"] = recorded_traffic(args.workload, STREAMK_PROFILES)
     if args.path == "3xtf32":
         tpk, tsrc = tf32_peak_tflops()
         roofline = {"bound": "tensor", "achieved": 3 * flop / per_launch_s / 1e12, "peak": tpk, "unit": "TFLOP/s",

@@ -95,6 +95,9 @@ _SIGNATURES = {
                                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "sgemm_f32_3xtf32_plan_model": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "sgemm_f32_streamk_plan_model": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
+                                                    ctypes.POINTER(ctypes.c_size_t)]),
 }
 
 _lock = threading.Lock()
@@ -360,6 +363,17 @@ def sgemm_f32_3xtf32_plan_model(M: int, N: int, K: int, sms: int):
     _check(load().sgemm_f32_3xtf32_plan_model(int(M), int(N), int(K), int(sms), ctypes.byref(w), ctypes.byref(s)),
            "sgemm_f32_3xtf32_plan_model")
     return int(w.value), int(s.value)
+
+
+def sgemm_f32_streamk_plan_model(M: int, N: int, K: int, sms: int, blocks_per_sm: int = 2):
+    """Test-only: (stream-K blocks, workspace bytes) of sgemm_f32_streamk for
+    an M x N x K product of aligned operands on a GPU with ``sms`` SMs and
+    ``blocks_per_sm`` resident blocks per SM; (0, 0) when it runs as
+    sgemm_f32.  Computed without a device."""
+    b, w = ctypes.c_longlong(0), ctypes.c_size_t(0)
+    _check(load().sgemm_f32_streamk_plan_model(int(M), int(N), int(K), int(sms), int(blocks_per_sm), ctypes.byref(b),
+                                               ctypes.byref(w)), "sgemm_f32_streamk_plan_model")
+    return int(b.value), int(w.value)
 
 
 def _rows(t, name):

@@ -1,5 +1,5 @@
 // Stream-K form of the TMA-fed FFMA kernel, for products whose tiles would
-// leave SMs idle (e.g. 1024^3: 64 tiles of 128 x 128 for 152 SMs).
+// leave SMs idle (e.g. 256 x 256 x 65536: 4 tiles of 128 x 128 for 152 SMs).
 //
 // "Shared Memory Tiling" ('What tiling does not fix') names the load
 // imbalance left when the tiles do not divide evenly over the SMs.  Here the
@@ -13,15 +13,20 @@
 // that share a tile (a segment):
 //  * a segment covering the whole tile stores it (alpha, beta epilogue);
 //  * otherwise the CTA writes its partial tile to its own slot of the
-//    workspace, then counts itself in on the tile's counter; the CTA that
-//    arrives last adds every segment's partial sums in k order (its own from
-//    registers) and stores the tile.  Whichever CTA arrives last, the sum is
-//    taken in the same order, so the result has the same bits on every run,
-//    and there is no wait on another CTA anywhere.
+//    workspace and counts itself in on the tile's counter.
+// When its run is done, a CTA waits (bounded) until every contributor of each
+// tile it shares has counted in, then adds up its own slice of that tile:
+// contributor j of n takes the 16-byte chunks [4096 j / n, 4096 (j + 1) / n)
+// and sums them over the n partial tiles in a fixed order -- k order, or, when
+// the slice is narrower than the CTA, k order within P groups of consecutive
+// contributors and then the P group sums in order -- and stores them.  The
+// order depends only on the shape, so every run gives the same bits, and the
+// whole grid shares the fix-up instead of one CTA per tile.  A CTA writes all
+// of its partial tiles before it waits on anything, and the grid is launched
+// cooperatively (every CTA resident at once), so every wait ends.
 // Each CTA has at most two partial segments (its first and its last), so the
 // workspace holds two partial tiles per CTA, plus one counter per tile that
-// the host zeroes before the launch.  The counters are reset by the last
-// arriver as well.
+// the host zeroes before the launch.
 #pragma once
 
 #include <cuda.h>
@@ -49,6 +54,88 @@ __device__ __forceinline__ int64_t streamk_chunk(int i, int q, int tid) {
     return ((int64_t)(i * (T::TN / 4) + q) * T::THREADS + tid) * 16;
 }
 
+// Thread 0 of a CTA: wait until *count reaches n (every contributor of a
+// shared tile has counted in), at most limit_ns; true if it did.  The load
+// after the count has been seen is ordered before the CTA's reads of the
+// partial tiles by the fence and the CTA barrier that follow.
+__device__ __forceinline__ bool wait_count_bounded(const int *count, int n, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(count) : "memory");
+        if (v >= n) {
+            __threadfence();
+            return v == n;
+        }
+        if (global_timer_ns() - t0 > limit_ns) return false;
+        __nanosleep(64);
+    }
+}
+
+// Contributor j of the n CTAs that share a tile: add up its slice of the
+// tile's 16-byte accumulator chunks over the n partial tiles (the first at
+// slot slot0, then the first slots of CTAs cf + 1, ..., cf + n - 1, in k
+// order) and store C = alpha * sum + beta * C there.  With fewer chunks in
+// the slice (m) than threads, P = THREADS / m groups of consecutive partial
+// tiles are summed side by side (each in k order) and the P sums are then
+// added in group order through `red` (P * m <= THREADS float4s); the order
+// depends only on (n, j), never on timing.  (tile_r, tile_c) is the tile's
+// corner in C.
+template <class T, bool VEC_C>
+__device__ __forceinline__ void streamk_fixup(const unsigned char *__restrict__ slots, int slot0, int cf, int n, int j,
+                                              float4 *red, int tile_r, int tile_c, float *__restrict__ C, int ldc,
+                                              int M, int N, float alpha, float beta) {
+    constexpr int64_t SLOT = (int64_t)T::BM * T::BN * 4;
+    constexpr int CHUNKS = T::TM * (T::TN / 4) * T::THREADS;
+    const int lo = (int)((int64_t)CHUNKS * j / n), hi = (int)((int64_t)CHUNKS * (j + 1) / n);
+    const int m = hi - lo;
+    if (m <= 0) return;
+    const int tid = threadIdx.x;
+    int P = m >= T::THREADS ? 1 : T::THREADS / m;
+    if (P > n) P = n;
+    // chunk g of a partial tile: accumulator chunk (i, q) of thread g % THREADS
+    auto part = [&](int r, int g) -> float4 {
+        const int64_t slot = r == 0 ? slot0 : 2 * (int64_t)(cf + r);
+        return __ldcg(reinterpret_cast<const float4 *>(slots + slot * SLOT + (int64_t)g * 16));
+    };
+    auto store = [&](int g, float4 v) {
+        const int th = g % T::THREADS, iq = g / T::THREADS;
+        const int i = iq / (T::TN / 4), q = iq % (T::TN / 4);
+        const int lane = th & 31, warp = th >> 5;
+        const int lm = (lane & 3) | (((lane >> 3) & 1) << 2);
+        const int ln = ((lane >> 2) & 1) | (((lane >> 4) & 1) << 1);
+        const int row = tile_r + (warp / T::WARPS_N) * T::WM + lm + 8 * i;
+        const int col = tile_c + (warp % T::WARPS_N) * T::WN + ln * 4 + 16 * q;
+        if (row >= M) return;
+        const float vp[4] = {v.x, v.y, v.z, v.w};
+        store_quad<VEC_C>(C + (int64_t)row * ldc, col, N, vp, alpha, beta);
+    };
+    auto add = [](float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
+    if (P == 1) {
+        for (int g = lo + tid; g < hi; g += T::THREADS) {
+            float4 v = part(0, g);
+#pragma unroll 8
+            for (int r = 1; r < n; ++r) v = add(v, part(r, g));
+            store(g, v);
+        }
+        return;
+    }
+    if (tid < P * m) {
+        const int g = lo + tid % m, p = tid / m;
+        const int r0 = n * p / P, r1 = n * (p + 1) / P;
+        float4 v = part(r0, g);
+#pragma unroll 8
+        for (int r = r0 + 1; r < r1; ++r) v = add(v, part(r, g));
+        red[p * m + tid % m] = v;
+    }
+    __syncthreads();
+    if (tid < m) {
+        float4 v = red[tid];
+        for (int p = 1; p < P; ++p) v = add(v, red[p * m + tid]);
+        store(lo + tid, v);
+    }
+}
+
 template <class T, bool VEC_C>
 __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     sgemm_ffma_tma_streamk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -58,8 +145,8 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     static_assert(T::PACKED, "the partial tiles are the packed accumulators");
     constexpr int64_t SLOT = (int64_t)T::BM * T::BN * 4;
     extern __shared__ unsigned char smem_raw[];
-    // values the k-loop does not need, kept out of its registers: the last
-    // arriver's flag, the partial tiles' bookkeeping, and thread 0's copy cursor
+    // values the k-loop does not need, kept out of its registers: the wait's
+    // outcome, the partial tiles' bookkeeping, and thread 0's copy cursor
     __shared__ int last_flag;
     __shared__ int info[4];        // cf_a, nseg_a, slot_a, nseg_b
     __shared__ int cursor[4];      // t_iss, k_iss, tm_iss, tn_iss
@@ -140,6 +227,7 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
     int it = 0;
     int failed_it = -1;
     int t = t_first, k = k_first;
+    int parts = 0;  // bit 0: the first tile is shared (written, counted); bit 1: the last one
     while (it < n_units) {
         const int seg = min(kt - k, n_units - it);
 #pragma unroll
@@ -183,48 +271,35 @@ __global__ void __launch_bounds__(T::THREADS, T::MIN_BLOCKS)
                        make_ulonglong2(acc2[i][2 * q], acc2[i][2 * q + 1]));
         __threadfence();
         __syncthreads();
-        const int cf = first_seg ? info[0] : (int)c;
-        const int n_seg = first_seg ? info[1] : info[3];
-        const int slot0 = first_seg ? info[2] : (int)(2 * c + 1);
-        if (tid == 0) {
-            const int prev = atomicAdd(counters + (t - 1), 1);
-            __threadfence();
-            last_flag = prev == n_seg - 1;
-            if (prev == n_seg - 1) counters[t - 1] = 0;  // ready for the next call
-        }
-        __syncthreads();
-        if (!last_flag) continue;
-        // the last to arrive: add the segments' partial sums in k order -- its
-        // own too, from the slot it has just written -- into the accumulators,
-        // one partial tile at a time with all of its loads in flight together
-        {
-            const unsigned char *src = slots + (int64_t)slot0 * SLOT + tid * 16;
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i)
-#pragma unroll
-                for (int q = 0; q < T::TN / 4; ++q) {
-                    const ulonglong2 w =
-                        __ldcg(reinterpret_cast<const ulonglong2 *>(src + (i * (T::TN / 4) + q) * T::THREADS * 16));
-                    acc2[i][2 * q] = w.x;
-                    acc2[i][2 * q + 1] = w.y;
-                }
-        }
-        const uint64_t one2 = f32x2_dup(1.f);
-        for (int r = 1; r < n_seg; ++r) {
-            // every segment after the first starts inside the tile: its CTA's first slot
-            const unsigned char *src = slots + (int64_t)(2 * (cf + r)) * SLOT + tid * 16;
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i)
-#pragma unroll
-                for (int q = 0; q < T::TN / 4; ++q) {
-                    const ulonglong2 w =
-                        __ldcg(reinterpret_cast<const ulonglong2 *>(src + (i * (T::TN / 4) + q) * T::THREADS * 16));
-                    f32x2_fma(acc2[i][2 * q], w.x, one2);  // s + v, rounded once (v * 1 is exact)
-                    f32x2_fma(acc2[i][2 * q + 1], w.y, one2);
-                }
-        }
-        store_tile<T, VEC_C, false>(acc, acc2, C, ldc, M, N, r0, c0, alpha, beta, 1, 0);
+        if (tid == 0) atomicAdd(counters + (t - 1), 1);
+        parts |= first_seg ? 1 : 2;
     }
+
+    // every partial tile of this CTA is written and counted: add up this
+    // CTA's slice of each, once all of the tile's contributors have counted in
+    bool gave_up = false;
+    if (failed_it < 0) {
+        float4 *red = reinterpret_cast<float4 *>(smem);  // the stage buffers are idle now
+        for (int which = 0; which < 2; ++which) {
+            if (!(parts & (1 << which))) continue;
+            const int tt = which == 0 ? t_first : t_last;
+            const int cf = which == 0 ? info[0] : (int)c;
+            const int n_seg = which == 0 ? info[1] : info[3];
+            const int slot0 = which == 0 ? info[2] : (int)(2 * c + 1);
+            if (tid == 0) last_flag = wait_count_bounded(counters + tt, n_seg, wait_limit_ns);
+            __syncthreads();
+            if (!last_flag) {
+                gave_up = true;
+                break;
+            }
+            int tm, tn;
+            grouped_tile<8>(tt, tiles_m, tiles_n, tm, tn);
+            streamk_fixup<T, VEC_C>(slots, slot0, cf, n_seg, (int)c - cf, red, tm * T::BM, tn * T::BN, C, ldc, M, N,
+                                    alpha, beta);
+            __syncthreads();  // red is reused for the second tile
+        }
+    }
+    if (gave_up && tid == 0) atomicCAS(err_word, kDeviceErrNone, kDeviceErrTimeout);
 
     if (failed_it >= 0 && tid == 0) {
         atomicCAS(err_word, kDeviceErrNone, kDeviceErrTimeout);

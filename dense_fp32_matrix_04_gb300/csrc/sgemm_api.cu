@@ -87,7 +87,7 @@ constexpr int kDebugNoOverlap = 512;  // launch the cluster-split grid without p
 constexpr int kDebugNoNarrow = 1024;
 constexpr int kDebugForcePhased = 2048;
 constexpr int kDebugForceStreamK = 4096;  // sgemm_f32_streamk: stream-K whatever the tile count
-constexpr int kDebugStreamKPerSmShift = 13;  // bits 13..14: stream-K blocks per SM (0 = one)
+constexpr int kDebugStreamKPerSmShift = 13;  // bits 13..14: stream-K blocks per SM (0 = all resident)
 std::atomic<int> g_debug_flags{0};
 // test-only (sgemm_test_tiny_path): tiny products take the one-thread-per-output kernel
 std::atomic<int> g_tiny_path{1};
@@ -759,44 +759,61 @@ int64_t streamk_resident(const DeviceInfo &info) {
 
 // How sgemm_f32_streamk runs a product: stream-K over a grid of `ctas` CTAs
 // (use == true), or sgemm_f32's own launch (no workspace).  Stream-K is taken
-// for TMA-addressable operands when sgemm_f32's plan (plain tiles, cluster
-// split, narrow tiles) would start fewer CTAs than the device has SMs -- few
-// output tiles over a long K, where at most eight CTAs can share a tile --
-// and then runs one CTA per SM.  Measured on GB300 (TFLOP/s, sgemm_f32 against
-// stream-K): 256 x 256 x 65536 22.3 / 41.0, 128 x 128 x 131072 5.6 / 17.8,
-// 384 x 384 x 16384 26.6 / 38.9; where sgemm_f32 fills the SMs stream-K was
-// not faster (1024^3 39.9 / 34.1, 2048^3 58.9 / 54, 512 x 512 x 32768 48.6 /
-// 50.4, 640 x 640 x 4096 44.1 / 37.9): two CTAs per SM pull apart (the older
-// one's warps issue first, the younger then runs alone) and each shared tile
-// costs a partial store and a fix-up.
+// for TMA-addressable operands with K > 64 (not tiny products) when
+//  * sgemm_f32's plan (plain tiles, cluster split, narrow tiles) would start
+//    fewer CTAs than the device has SMs -- few output tiles over a long K,
+//    where at most eight CTAs can share a tile; or
+//  * the product has fewer 128 x 128 tiles than SMs and every resident block
+//    gets at least kStreamKMinUnits (tile, k-step) units.
+// It then runs every resident block (two per SM).  Measured on GB300
+// (TFLOP/s, sgemm_f32 against stream-K at two blocks per SM): 256 x 256 x
+// 65536 22.2 / 54.5, 128 x 128 x 131072 5.7 / 46.6, 384 x 384 x 4096 22.5 /
+// 28.8, 512 x 512 x 16384 47.1 / 55.6 (26.9 units per block), 1024 x 1024 x
+// 4096 48.6 / 50.8 (26.9), 1024 x 1024 x 8192 50.8 / 56.5, 1280 x 1280 x 8192
+// 53.7 / 57.9; below the threshold sgemm_f32 holds its own or wins: 1024 x
+// 1024 x 2048 44.8 / 41.5 (13.5 units), 1536^3 51.8 / 47.8 (22.7), 768 x 768
+// x 4096 49.9 / 47.7 (15.2), 1024^3 39.8 / 32.3 (6.7); with more tiles than
+// SMs stream-K was not faster either (2048 x 2048 x 8192 62.4 / 60.7).
+constexpr int64_t kStreamKMinUnits = 24;
+
 struct StreamKPlan {
     bool use = false;
     int64_t tiles = 0, ctas = 0;
     size_t counter_bytes = 0, bytes = 0;
 };
 
-StreamKPlan streamk_plan(const Problem &p, const DeviceInfo &info) {
+// The decision and the grid without a device: `sms` SMs, `resident` blocks of
+// the stream-K kernel resident at once, `dbg` the test-only switches, fits()
+// as for split_plan_model.
+template <class Fits>
+StreamKPlan streamk_plan_model(int M, int N, int K, int64_t sms, int64_t resident, int dbg, Fits fits) {
     using T = StreamKTile;
     StreamKPlan plan;
-    if (!use_tma(p) || (int64_t)p.M * p.N == 0 || p.K <= 2 * TmaSmallK::BK) return plan;
-    plan.tiles = (int64_t)((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN);
-    const int dbg = g_debug_flags.load();
+    if ((int64_t)M * N == 0 || K <= 2 * TmaSmallK::BK || resident <= 0) return plan;
+    plan.tiles = (int64_t)((M + T::BM - 1) / T::BM) * ((N + T::BN - 1) / T::BN);
+    const int64_t units = plan.tiles * ((K + T::BK - 1) / T::BK);
     if (!(dbg & kDebugForceStreamK)) {
-        const SplitPlan sp = split_plan(p.M, p.N, p.K, info, Narrow::kTma);
+        const SplitPlan sp = split_plan_model(M, N, K, sms, Narrow::kTma, dbg, fits);
         const int64_t ctas = sp.narrow ? sp.tiles * sp.cs : sp.full + (sp.tiles - sp.full) * sp.cs;
-        if (ctas >= info.sms) return plan;
+        const bool long_k = plan.tiles < sms && units >= kStreamKMinUnits * resident;
+        if (ctas >= sms && !long_k) return plan;
     }
-    int64_t resident = streamk_resident<T>(info);
-    if (resident <= 0) return plan;
     const int forced = (dbg >> kDebugStreamKPerSmShift) & 3;
-    const int64_t want = (int64_t)(forced > 0 ? forced : 1) * info.sms;
-    if (want < resident) resident = want;
-    const int64_t units = plan.tiles * k_tiles(p);
+    if (forced > 0 && forced * sms < resident) resident = forced * sms;
     plan.use = true;
     plan.ctas = units < resident ? units : resident;
     plan.counter_bytes = (size_t)((plan.tiles * 4 + 255) / 256 * 256);
     plan.bytes = plan.counter_bytes + (size_t)(2 * plan.ctas) * T::BM * T::BN * 4;
     return plan;
+}
+
+StreamKPlan streamk_plan(const Problem &p, const DeviceInfo &info) {
+    if (!use_tma(p) || tiny_product(p)) return StreamKPlan{};
+    const int64_t resident = streamk_resident<StreamKTile>(info);
+    auto fits = [&](bool narrow_tile, int c) {
+        return narrow_tile ? cluster_fits<TmaNarrow>(info.dev, c) : cluster_fits<TmaTile>(info.dev, c);
+    };
+    return streamk_plan_model(p.M, p.N, p.K, info.sms, resident, g_debug_flags.load(), fits);
 }
 
 int launch_streamk(const Problem &p, const StreamKPlan &plan, void *workspace, cudaStream_t stream,
@@ -811,10 +828,27 @@ int launch_streamk(const Problem &p, const StreamKPlan &plan, void *workspace, c
     if (cudaMemsetAsync(counters, 0, (size_t)plan.tiles * 4, stream) != cudaSuccess) return SGEMM_ERR_LAUNCH;
     const bool vc = aligned16(p.C) && p.ldc % 4 == 0;
     auto kernel = vc ? sgemm::sgemm_ffma_tma_streamk_kernel<T, true> : sgemm::sgemm_ffma_tma_streamk_kernel<T, false>;
-    kernel<<<(unsigned)plan.ctas, T::THREADS, T::SMEM_BYTES, stream>>>(
-        ta, tb, p.M, p.N, p.K, p.alpha, p.beta, p.C, p.ldc, counters, slots, info.err_word, g_wait_limit_ns.load(),
-        g_debug_flags.load());
-    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+    // cooperative: the CTAs that share a tile wait for one another's partial
+    // tiles at the end of their runs, so all of them must be resident at once
+    // (the grid is at most the resident count; the launch fails otherwise)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.ctas);
+    cfg.blockDim = dim3(T::THREADS);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, p.M, p.N, p.K, p.alpha, p.beta, p.C, p.ldc, counters,
+                                             slots, info.err_word, (unsigned long long)g_wait_limit_ns.load(),
+                                             g_debug_flags.load());
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
 }
 
 // Byte range [lo, hi) spanned by a rows x cols matrix with leading dimension ld.
@@ -1126,6 +1160,22 @@ int sgemm_f32_plan_model(int M, int N, int K, int path, int sms, long long *tile
         return split_plan_model(M, N, K, sms, narrow, 0, [](bool, int) { return true; });
     };
     return report_plan(M, N, K, path, model, tiles, full_tiles, cluster_size, tile_n);
+}
+
+int sgemm_f32_streamk_plan_model(int M, int N, int K, int sms, int blocks_per_sm, long long *blocks,
+                                 size_t *workspace_bytes) {
+    if (!blocks || !workspace_bytes || M < 0 || N < 0 || K < 0 || sms < 1 || blocks_per_sm < 1)
+        return SGEMM_ERR_INVALID_ARG;
+    *blocks = 0;
+    *workspace_bytes = 0;
+    if (tiny_product(Problem{M, N, K, nullptr, 1, nullptr, 1, nullptr, 1})) return SGEMM_OK;
+    const StreamKPlan plan =
+        streamk_plan_model(M, N, K, sms, (int64_t)sms * blocks_per_sm, 0, [](bool, int) { return true; });
+    if (plan.use) {
+        *blocks = plan.ctas;
+        *workspace_bytes = plan.bytes;
+    }
+    return SGEMM_OK;
 }
 
 size_t sgemm_f32_splitk_workspace_size(int M, int N, int splits) { return partials_bytes(M, N, splits); }

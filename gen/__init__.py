@@ -132,7 +132,8 @@ def strided(mat: np.ndarray, ld: int, fill: float = np.nan) -> np.ndarray:
     return buf
 
 
-#: The synthetic workloads, by name: the five of the pages' examples and one larger square product.
+#: The synthetic workloads, by name: the five of the pages' examples, one larger square product
+#: and one long-K product with few output tiles.
 #: Each entry: (M, N, K, dist, seed).
 WORKLOADS = {
     "tiny_6x6x9": (6, 6, 9, "uniform", 0),
@@ -143,4 +144,7 @@ WORKLOADS = {
     # not one of the pages' examples: the headline's square product at twice
     # the size, where the FP32 kernel's L2 reuse is tested hardest
     "square_16384": (16384, 16384, 16384, "normal", 5),
+    # not one of the pages' examples: four output tiles over a long K, the
+    # load imbalance that tiling alone leaves (few tiles for many SMs)
+    "longk_256x256x65536": (256, 256, 65536, "uniform", 6),
 }

@@ -183,26 +183,32 @@ int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
  * K (e.g. 256 x 256 x 65536), where even thread-block clusters of eight
  * blocks per tile would leave SMs idle -- the load imbalance "Shared Memory
  * Tiling" ('What tiling does not fix') points at.  The product is cut into
- * units of one 128 x 128 tile and one 32-deep k-step, and one block per SM
- * takes an equal contiguous run of them across tile boundaries, with the
- * tiled kernel of sgemm_f32 (TMA-fed tiles, packed FP32 FMAs).  A tile shared
- * by several blocks is finished by whichever arrives last: it adds the
- * partial tiles in k order (so every run gives the same bits) and stores the
- * tile.  Each element is an FP32 sum of FP32 products within the bound
+ * units of one 128 x 128 tile and one 32-deep k-step, and every block that
+ * can be resident (two per SM) takes an equal contiguous run of them across
+ * tile boundaries, with the tiled kernel of sgemm_f32 (TMA-fed tiles, packed
+ * FP32 FMAs).  The blocks that share a tile write their partial tiles to the
+ * workspace; once all have, each adds up its own slice of the tile over them
+ * in an order fixed by the shape (so every run gives the same bits) and
+ * stores it.  Each element is an FP32 sum of FP32 products within the bound
  * stated above, and exact for small integers.
  *   Stream-K runs when A and B are 16-byte aligned with leading dimensions
- *   that are multiples of 4, K > 64, and sgemm_f32's own plan would start
- *   fewer blocks than the device has SMs.  Every other product runs exactly
- *   as sgemm_f32 does and reads no workspace.
+ *   that are multiples of 4, K > 64, the product is not a tiny one (see
+ *   sgemm_f32), and either sgemm_f32's own plan would start fewer blocks than
+ *   the device has SMs, or there are fewer 128 x 128 tiles than SMs and each
+ *   block gets at least 24 units.  Every other product runs exactly as
+ *   sgemm_f32 does and reads no workspace.  The kernel is launched
+ *   cooperatively (all of its blocks resident at once).
  *   workspace: caller-owned device memory of at least
  *     sgemm_f32_streamk_workspace_size(M, N, K) bytes (0 when the product
- *     does not take stream-K), 16-byte aligned, not overlapping A, B or C: one
- *     counter per tile, which the call zeroes (a memset on `stream`) before
- *     its kernel, and two partial tiles per block.  Its contents on entry do
- *     not matter.  Calls that share a workspace must not overlap on the GPU.
- * Errors as for sgemm_f32_splitk.  The copy waits are bounded; a block that
- * gives up stops, so the tiles it shares are not stored (C keeps its old
- * values there) and sgemm_device_status reports SGEMM_ERR_TIMEOUT.
+ *     does not take stream-K; about 40 MB on a GPU with 152 SMs), 16-byte
+ *     aligned, not overlapping A, B or C: one counter per tile, which the call
+ *     zeroes (a memset on `stream`) before its kernel, and two partial tiles
+ *     per block.  Its contents on entry do not matter.  Calls that share a
+ *     workspace must not overlap on the GPU.
+ * Errors as for sgemm_f32_splitk.  Every wait is bounded -- on the copies, and
+ * on the other blocks that share a tile; a block that gives up stops, so the
+ * tiles it shares are not stored (C keeps its old values there) and
+ * sgemm_device_status reports SGEMM_ERR_TIMEOUT.
  */
 int sgemm_f32_streamk(int M, int N, int K,
                       const float *A, int lda,

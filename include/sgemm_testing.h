@@ -10,6 +10,8 @@
 #ifndef SGEMM_TESTING_H
 #define SGEMM_TESTING_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -33,7 +35,7 @@ extern "C" {
  * operands through the phase maps too (every shift 0), so the phased kernel
  * can be checked on any inputs; bit 12: sgemm_f32_streamk takes stream-K
  * whenever its operands allow it; bits 13..14: its grid holds that many blocks
- * per SM (0 = one).
+ * per SM (0 = every block that can be resident, two per SM).
  * wait_limit_ns: the bound of each wait (default 2 s).
  * flags = 0 and wait_limit_ns = 2000000000 restore the defaults.
  * SGEMM_ERR_INVALID_ARG if flags < 0, wait_limit_ns == 0, or the environment
@@ -74,12 +76,26 @@ int sgemm_f32_plan_model(int M, int N, int K, int path, int sms, long long *tile
 /*
  * How sgemm_f32_3xtf32 lays out an M x N x K product on a GPU with `sms`
  * SMs, without a device: *tile_n = the width of its 128-row output tiles
- * (256 down to 128 in steps of 16, the width that fills the last round of
- * tiles over the SMs best) and *splits = the number of CTA rows that divide
- * the k-steps of a small grid (1: none).  SGEMM_ERR_INVALID_ARG for a NULL
- * output, a negative size or sms < 1.
+ * (208 down to 128 in steps of 16, the width with the lowest estimated cost:
+ * rounds of tiles over the SMs x (width + 128) x k-steps per part) and
+ * *splits = the number of parts that divide the k-steps of a small grid
+ * (1: none).  SGEMM_ERR_INVALID_ARG for a NULL output, a negative size or
+ * sms < 1.
  */
 int sgemm_f32_3xtf32_plan_model(int M, int N, int K, int sms, int *tile_n, int *splits);
+
+/*
+ * How sgemm_f32_streamk runs an M x N x K product of 16-byte aligned
+ * operands on a GPU with `sms` SMs where `blocks_per_sm` blocks of its kernel
+ * can be resident, without a device: *blocks = the stream-K grid (0: the call
+ * runs as sgemm_f32) and *workspace_bytes = what sgemm_f32_streamk_workspace_size
+ * would return there.  Every cluster size is assumed resident and every test
+ * switch off (the tiny-product path follows sgemm_test_tiny_path).
+ * SGEMM_ERR_INVALID_ARG for a NULL output, a negative size, sms < 1 or
+ * blocks_per_sm < 1.
+ */
+int sgemm_f32_streamk_plan_model(int M, int N, int K, int sms, int blocks_per_sm, long long *blocks,
+                                 size_t *workspace_bytes);
 
 #ifdef __cplusplus
 }

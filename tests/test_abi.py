@@ -25,7 +25,8 @@ def declared_functions(headers=None):
 
 
 # the test-only interface lives in its own header, never in the product's
-TEST_ONLY = {"sgemm_test_switches", "sgemm_test_tiny_path", "sgemm_f32_plan_model", "sgemm_f32_3xtf32_plan_model"}
+TEST_ONLY = {"sgemm_test_switches", "sgemm_test_tiny_path", "sgemm_f32_plan_model", "sgemm_f32_3xtf32_plan_model",
+             "sgemm_f32_streamk_plan_model"}
 
 
 @pytest.fixture(scope="module")

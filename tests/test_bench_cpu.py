@@ -58,9 +58,13 @@ def test_recorded_traffic_follows_the_kernel_sources():
     assert t0 is None or t0 < 1_000_000
     assert bench.recorded_traffic("no_such_workload") is None
     assert len(bench.kernel_source_digest()) == 16
-    for name, sources, tile in bench.TRAFFIC_PROFILES.values():
+    for name, sources, tile in list(bench.TRAFFIC_PROFILES.values()) + list(bench.STREAMK_PROFILES.values()):
         assert os.path.exists(os.path.join(bench.ROOT, "profiles", name))
         assert len(bench.kernel_source_digest(sources, tile)) == 16
+    # the stream-K kernel's profile is looked up in its own table: at least A and B come from DRAM
+    sk = bench.recorded_traffic("longk_256x256x65536", bench.STREAMK_PROFILES)
+    assert sk is None or sk > 4 * 2 * 256 * 65536
+    assert bench.recorded_traffic("longk_256x256x65536") is None
     # comments do not enter the digest; code does
     assert bench.code_only("int a; // x\n/* y\n z */ int  b;") == bench.code_only("int a;\nint b; // other")
     assert bench.code_only("int a;") != bench.code_only("int b;")

@@ -192,3 +192,56 @@ def test_3xtf32_layout_follows_the_rule():
     (1024, 1024, 1024, (176, 3))])
 def test_3xtf32_layout_on_the_workloads(M, N, K, want):
     assert sg.sgemm_f32_3xtf32_plan_model(M, N, K, SMS) == want
+
+
+# ---------------------------------------------------------------- stream-K decision
+
+# sgemm_f32 against stream-K at two blocks per SM (TFLOP/s, CUDA events,
+# medians; GB300, 152 SMs, L2 flushed between calls): the shapes stream-K
+# takes, with both rates, and the shapes it leaves to sgemm_f32
+STREAMK_TAKEN = [
+    (256, 256, 65536, 22.2, 54.5), (128, 128, 131072, 5.7, 46.6), (384, 384, 16384, 26.4, 47.7),
+    (256, 512, 32768, 24.3, 55.6), (384, 384, 4096, 22.5, 28.8), (256, 256, 8192, 18.8, 28.3),
+    (128, 1024, 16384, 23.5, 48.0), (512, 512, 32768, 48.4, 58.7), (512, 512, 16384, 47.1, 55.6),
+    (1024, 1024, 4096, 48.6, 50.8), (1024, 1024, 8192, 50.8, 56.5), (640, 640, 16384, 50.7, 55.1),
+    (1280, 1280, 8192, 53.7, 57.9), (896, 896, 8192, 49.7, 53.8), (512, 2048, 8192, 50.8, 55.9),
+    (768, 768, 8192, 54.0, 54.3), (1536, 1536, 4096, 56.1, 56.3),
+]
+STREAMK_LEFT = [
+    (1024, 1024, 1024, 39.8, 32.3), (2048, 2048, 2048, 58.9, 55.9), (640, 640, 4096, 44.0, 40.5),
+    (768, 768, 4096, 49.9, 47.7), (1024, 1024, 2048, 44.8, 41.5), (1536, 1536, 1536, 51.8, 47.8),
+    (2048, 2048, 8192, 62.4, 60.7), (1280, 1280, 2048, 47.9, 48.2), (300, 700, 10000, 35.2, 35.4),
+]
+
+
+@pytest.mark.parametrize("M,N,K,f32,sk", STREAMK_TAKEN)
+def test_streamk_taken_where_measured_faster(M, N, K, f32, sk):
+    assert sk >= (1 - NEAR) * f32
+    blocks, ws = sg.sgemm_f32_streamk_plan_model(M, N, K, SMS)
+    units = tiles128(M, N) * -(-K // 32)
+    assert blocks == min(units, 2 * SMS)
+    # a counter per tile (in 256-byte blocks) and two 128 x 128 partial tiles per block
+    assert ws == -(-tiles128(M, N) * 4 // 256) * 256 + 2 * blocks * 128 * 128 * 4
+
+
+@pytest.mark.parametrize("M,N,K,f32,sk", STREAMK_LEFT)
+def test_streamk_left_to_sgemm_f32_where_not_faster(M, N, K, f32, sk):
+    assert sk <= (1 + NEAR) * f32
+    assert sg.sgemm_f32_streamk_plan_model(M, N, K, SMS) == (0, 0)
+
+
+def test_streamk_limits():
+    # K <= 64 and tiny products never take stream-K; the grid follows the blocks per SM
+    assert sg.sgemm_f32_streamk_plan_model(256, 256, 64, SMS) == (0, 0)
+    assert sg.sgemm_f32_streamk_plan_model(100, 100, 100, SMS) == (0, 0)
+    assert sg.sgemm_f32_streamk_plan_model(256, 256, 65536, SMS, 1)[0] == SMS
+    assert sg.sgemm_f32_streamk_plan_model(128, 128, 96, SMS)[0] == 0          # tiny: 16384 outputs, K <= 128
+    sg.sgemm_test_tiny_path(False)
+    try:
+        assert sg.sgemm_f32_streamk_plan_model(128, 128, 96, SMS)[0] == 3     # one tile of three k-steps
+    finally:
+        sg.sgemm_test_tiny_path(True)
+    import ctypes
+    b, w = ctypes.c_longlong(), ctypes.c_size_t()
+    for args in [(-1, 4, 4, SMS, 2), (4, 4, 4, 0, 2), (4, 4, 4, SMS, 0)]:
+        assert sg.load().sgemm_f32_streamk_plan_model(*args, ctypes.byref(b), ctypes.byref(w)) == sg.SGEMM_ERR_INVALID_ARG

@@ -1,11 +1,13 @@
 """sgemm_f32_streamk: the product cut into (tile, 32-deep k-step) units dealt
-evenly to one block per SM, partial tiles added in k order by the block that
-finishes each shared tile.  Parity with the FP64 oracle on every element (the
-long-K shapes it is planned for, and other shapes with stream-K forced by a
-test-only switch, at one and two blocks per SM), exact small integers, the
-same bits on every run, the workspace contract (canaries around it, garbage
-on entry, errors), the fall-back to sgemm_f32's own launch, and the
-bounded-wait path."""
+evenly to every resident block (two per SM); the blocks that share a tile
+each add up their own slice of its partial tiles, in an order fixed by the
+shape (in k order, or in groups of consecutive partial tiles when a tile has
+more sharers than its slices have chunks per thread).  Parity with the FP64
+oracle on every element (the long-K shapes it is planned for, and other
+shapes with stream-K forced by a test-only switch, at one and two blocks per
+SM), exact small integers, the same bits on every run, the workspace
+contract (canaries around it, garbage on entry, errors), the fall-back to
+sgemm_f32's own launch, and the bounded-wait path."""
 
 import numpy as np
 import pytest
@@ -16,6 +18,7 @@ from helpers import CANARY_BITS, GUARD, WS_GUARD, _device_buffer, check_full
 pytestmark = pytest.mark.gpu
 
 FORCE_STREAMK = 4096
+ONE_PER_SM = 1 << 13
 TWO_PER_SM = 2 << 13
 
 
@@ -67,15 +70,24 @@ def run_streamk(sg, A, B, lda=None, ldb=None, ldc=None, c_off=0, ws_fill=float("
     return C
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 65536), (128, 128, 131072), (384, 384, 16384), (130, 250, 20000)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 65536), (128, 128, 131072), (384, 384, 16384), (130, 250, 20000),
+                                   (1024, 1024, 8192), (520, 500, 16384)])
 def test_planned_long_k_shapes(sg, M, N, K):
     A, B = gen.operands(M, N, K, seed=500 + M % 97)
     check_full(run_streamk(sg, A, B, expect_ws=True), A, B)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 65536), (1024, 1024, 8192), (1024, 1024, 1024), (128, 128, 96),
+                                   (512, 512, 16384), (2048, 2048, 8192), (384, 384, 4096)])
+def test_device_plan_matches_the_model(sg, M, N, K):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sg.sgemm_f32_streamk_workspace_size(M, N, K) == sg.sgemm_f32_streamk_plan_model(M, N, K, sms, 2)[1]
+
+
 @pytest.fixture(params=["one-per-sm", "two-per-sm"])
 def forced(request, sg):
-    sg.sgemm_test_switches(FORCE_STREAMK | (TWO_PER_SM if request.param == "two-per-sm" else 0))
+    sg.sgemm_test_switches(FORCE_STREAMK | (TWO_PER_SM if request.param == "two-per-sm" else ONE_PER_SM))
     return request.param
 
 
@@ -98,8 +110,12 @@ def test_integers_exact(sg):
     check_full(run_streamk(sg, A, B, expect_ws=True), A, B, exact=True)
 
 
-def test_same_bits_every_run_and_garbage_workspace(sg):
-    A, B = gen.operands(256, 384, 20000, seed=502)
+@pytest.mark.parametrize("M,N,K", [
+    (256, 384, 20000),    # 6 tiles, about 51 sharers each: every slice summed in k order
+    (128, 128, 65536),    # 1 tile, 304 sharers: slices of 13-14 chunks summed in 9 groups
+])
+def test_same_bits_every_run_and_garbage_workspace(sg, M, N, K):
+    A, B = gen.operands(M, N, K, seed=502)
     c1 = run_streamk(sg, A, B, ws_fill=0.0)
     c2 = run_streamk(sg, A, B, ws_fill="garbage")   # counters start at 0x7fffffff: the call zeroes them
     c3 = run_streamk(sg, A, B)
