@@ -72,6 +72,7 @@ TRAFFIC_PROFILES = {
     "square_16384": ("ffma_tma_square_16384.md", KERNEL_SOURCES, "TmaMainTile"),
     "tiny_6x6x9": ("ffma_tiny_6x6x9.md", ["dense_fp32_matrix_04_gb300/csrc/ffma_tiny.cuh",
                                           "dense_fp32_matrix_04_gb300/csrc/epilogue.cuh"], None),
+    "longk_256x256x65536": ("ffma_narrow_longk_256x256x65536.md", KERNEL_SOURCES, "TmaNarrowTile"),
 }
 # the same for sgemm_f32_streamk's kernel, on the workloads that take it
 STREAMK_PROFILES = {

@@ -64,7 +64,8 @@ def test_recorded_traffic_follows_the_kernel_sources():
     # the stream-K kernel's profile is looked up in its own table: at least A and B come from DRAM
     sk = bench.recorded_traffic("longk_256x256x65536", bench.STREAMK_PROFILES)
     assert sk is None or sk > 4 * 2 * 256 * 65536
-    assert bench.recorded_traffic("longk_256x256x65536") is None
+    lk = bench.recorded_traffic("longk_256x256x65536")
+    assert lk is None or lk > 4 * 2 * 256 * 65536
     # comments do not enter the digest; code does
     assert bench.code_only("int a; // x\n/* y\n z */ int  b;") == bench.code_only("int a;\nint b; // other")
     assert bench.code_only("int a;") != bench.code_only("int b;")
