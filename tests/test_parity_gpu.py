@@ -100,6 +100,32 @@ def test_skinny_16384x16384x32_full(sg):
     check_full_blocked(C, A, B, key="skinny_16384x16384x32")
 
 
+def test_square_16384_sampled(sg):
+    # the headline's product at twice the size (not one of the pages'
+    # examples): every output finite, whole rows at tile edges and 2000 random
+    # entries against the oracle.  Every one of its 2^28 outputs passed once
+    # (max error/bound 2.3e-4), but the oracle takes five minutes on 16 cores
+    M, N, K, dist, seed = gen.WORKLOADS["square_16384"]
+    A, B = gen.operands(M, N, K, seed=seed, dist=dist)
+    C = _device_product(sg, A, B)
+    assert np.isfinite(C).all()
+    check_rows(C, A, B, [0, 127, 128, 8191, 8192, 16383])
+    check_entries(C, A, B, *_sample(M, N, np.random.default_rng(5), 2000))
+
+
+def test_longk_256x256x65536_full(sg):
+    # four output tiles over 65536 k-values: sgemm_f32's narrow tiles, each
+    # split over a cluster of eight CTAs; and the same product through stream-K
+    import torch
+    M, N, K, dist, seed = gen.WORKLOADS["longk_256x256x65536"]
+    A, B = workload_operands("longk_256x256x65536")
+    C = _device_product(sg, A, B)
+    check_full_blocked(C, A, B, key="longk_256x256x65536")
+    Cs = sg.matmul_streamk(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()).cpu().numpy()
+    assert sg.sgemm_f32_streamk_workspace_size(M, N, K) > 0
+    check_full_blocked(Cs, A, B, key="longk_256x256x65536")
+
+
 # ------------------------------------------------------------------ exactness
 
 def test_integer_inputs_exact_multi_tile(sg, path):
