@@ -423,6 +423,10 @@ def kernel_name(sg, M, N, K):
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed small-K tile, 1 stage, 8x8 per thread as "
                     "fma.rn.f32x2 column pairs, k-groups unrolled by 8, 4 CTAs/SM)")
         tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
+        if tn == 64 and cs == 1:
+            return (f"sgemm_ffma_tma_ksplit_kernel (one round of {tiles} 128x64x32 TMA-fed tiles, one CTA each of two "
+                    "groups of two warps on alternate k-steps, a 4-stage ring, 8x16 per thread as fma.rn.f32x2 "
+                    "column pairs; the groups' sums added through shared memory)")
         if tn == 64:
             return ("sgemm_ffma_tma_kernel (128x64x32 TMA-fed narrow tile, 2 stages, 8x8 per thread as "
                     f"fma.rn.f32x2 column pairs, 4 CTAs/SM); all {tiles} tiles split over {cs}-CTA clusters "

@@ -39,6 +39,7 @@
 #include "ffma_tma_phased.cuh"
 #include "ffma_tma_sgemm.cuh"
 #include "ffma_tma_smallk.cuh"
+#include "ffma_tma_ksplit.cuh"
 #include "ffma_tma_streamk.cuh"
 #include "ffma_tiny.cuh"
 #include "ladder.cuh"
@@ -65,6 +66,7 @@ using TmaSmallK = sgemm::TmaSmallKTile;
 using TmaSmallK1 = sgemm::TmaSmallK1Tile;
 using TmaNarrow = sgemm::TmaNarrowTile;
 using TmaNarrowCp = sgemm::TmaNarrowCpTile;
+using TmaKSplit = sgemm::TmaKSplitTile;
 using TmaPhased = sgemm::PhasedTile<sgemm::TmaMainTile>;
 using PhasedNarrow = sgemm::PhasedTile<sgemm::TmaNarrowTile>;
 using X3Tile = sgemm::Tf32x3MainTile;
@@ -229,10 +231,10 @@ bool cp_fits(const Problem &p) { return 4 * (int64_t)p.lda <= kIntMax; }
 // only when every stride of either width fits.
 bool cp_narrow_fits(const Problem &p) { return 16 * (int64_t)p.lda <= kIntMax && 8 * (int64_t)p.ldb <= kIntMax; }
 
-template <class T, bool VC, int ROLE>
+template <class T, bool VC, int ROLE, bool PLAIN = false>
 bool tma_attr(int dev) {
     static std::atomic<int> done[kMaxDevices];
-    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC, ROLE>, T::SMEM_BYTES);
+    return smem_attr_once(done[dev], sgemm::sgemm_ffma_tma_kernel<T, VC, ROLE, PLAIN>, T::SMEM_BYTES);
 }
 
 template <class T, bool VC, int ROLE>
@@ -313,7 +315,17 @@ struct SplitPlan {
     int64_t full = 0;
     int cs = 1;
     bool narrow = false;  // tiles are the narrow tile's (128 x 64), all of them in clusters of cs
+    bool ksplit = false;  // narrow tiles, one CTA each of two warp groups on alternate k-steps (cs == 1)
 };
+
+// The k-split tile (ffma_tma_ksplit.cuh) takes TMA products with fewer main
+// tiles than SMs whose 128 x 64 tiles fill one round over the SMs to at least
+// kKSplitFillPct (70 %), with at most kKSplitMaxSteps (48) k-steps: there it
+// beat the narrow tile's cluster plan by 1-22 % on GB300 (1024^3: 52.8
+// against 54.0 us; 1024 x 1216 x 1024: 52.8 against 64.3), and lost beyond
+// those bounds (96 tiles on 152 SMs; 64 k-steps: 97.7 against 95.5 us).
+constexpr int64_t kKSplitFillPct = 70;
+constexpr int64_t kKSplitMaxSteps = 48;
 
 // Cost model of the main tile, fitted to measurements on GB300 of products from
 // 512 x 512 x 8192 to 8192^3: two CTAs on an SM each advance one k-step per
@@ -398,6 +410,13 @@ SplitPlan split_plan_model(int M, int N, int K, int64_t sms, Narrow narrow, int 
             using TN = TmaNarrow;
             const NarrowModel &m = narrow == Narrow::kCp ? kNarrowCp : kNarrowTma;
             const int64_t ntiles = (int64_t)((M + TN::BM - 1) / TN::BM) * ((N + TN::BN - 1) / TN::BN);
+            static_assert(TmaKSplit::BM == TN::BM && TmaKSplit::BN == TN::BN, "one narrow tile shape");
+            if (narrow == Narrow::kTma && ntiles <= P && 100 * ntiles >= kKSplitFillPct * P && kt <= kKSplitMaxSteps) {
+                plan.tiles = plan.full = ntiles;
+                plan.cs = 1;
+                plan.narrow = plan.ksplit = true;
+                return plan;
+            }
             int ncs = 0;
             double nbest = 0.0;
             for (int c = 2; c <= 8 && kt >= 4 * c; c *= 2) {
@@ -437,9 +456,9 @@ SplitPlan split_plan(int M, int N, int K, const DeviceInfo &info, Narrow narrow,
 // Launch the TMA kernel over grouped tiles [tile_base, tile_base + tiles): a
 // plain (tiles x splits) grid, the same as the first of a plain + split pair
 // (primary), or tiles clusters of cs CTAs (cs > 1).
-template <class T>
-int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
-               int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
+template <class T, bool PLAIN>
+int launch_tma_as(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
+                  int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
     alignas(64) CUtensorMap ta, tb;
     if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -457,20 +476,21 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
             if constexpr (!T::CSPLIT_OK) {
                 return SGEMM_ERR_LAUNCH;  // only a tile that supports the cluster split has a split to precede
             } else {
-                if (!(vc ? tma_attr<T, true, sgemm::kRolePrimary>(info.dev)
-                         : tma_attr<T, false, sgemm::kRolePrimary>(info.dev)))
+                if (!(vc ? tma_attr<T, true, sgemm::kRolePrimary, PLAIN>(info.dev)
+                         : tma_attr<T, false, sgemm::kRolePrimary, PLAIN>(info.dev)))
                     return SGEMM_ERR_LAUNCH;
-                auto kernel = vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRolePrimary>
-                                 : sgemm_ffma_tma_kernel<T, false, sgemm::kRolePrimary>;
+                auto kernel = vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRolePrimary, PLAIN>
+                                 : sgemm_ffma_tma_kernel<T, false, sgemm::kRolePrimary, PLAIN>;
                 kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc,
                                                                     partials, ldp, (int)tile_base, info.err_word, wait,
                                                                     dbg);
             }
         } else {
-            if (!(vc ? tma_attr<T, true, sgemm::kRolePlain>(info.dev) : tma_attr<T, false, sgemm::kRolePlain>(info.dev)))
+            if (!(vc ? tma_attr<T, true, sgemm::kRolePlain, PLAIN>(info.dev)
+                     : tma_attr<T, false, sgemm::kRolePlain, PLAIN>(info.dev)))
                 return SGEMM_ERR_LAUNCH;
-            auto kernel = vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRolePlain>
-                             : sgemm_ffma_tma_kernel<T, false, sgemm::kRolePlain>;
+            auto kernel = vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRolePlain, PLAIN>
+                             : sgemm_ffma_tma_kernel<T, false, sgemm::kRolePlain, PLAIN>;
             kernel<<<grid, T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc,
                                                                 partials, ldp, (int)tile_base, info.err_word, wait, dbg);
         }
@@ -479,10 +499,12 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
     if constexpr (!T::CSPLIT_OK) {
         return SGEMM_ERR_LAUNCH;
     } else {
-        if (!(vc ? tma_attr<T, true, sgemm::kRoleSplit>(info.dev) : tma_attr<T, false, sgemm::kRoleSplit>(info.dev)))
+        if (!(vc ? tma_attr<T, true, sgemm::kRoleSplit, PLAIN>(info.dev)
+                 : tma_attr<T, false, sgemm::kRoleSplit, PLAIN>(info.dev)))
             return SGEMM_ERR_LAUNCH;
         auto kernel =
-            vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit> : sgemm_ffma_tma_kernel<T, false, sgemm::kRoleSplit>;
+            vc ? sgemm_ffma_tma_kernel<T, true, sgemm::kRoleSplit, PLAIN>
+               : sgemm_ffma_tma_kernel<T, false, sgemm::kRoleSplit, PLAIN>;
         // behind a plain grid of the same product: start on the SMs it frees as it drains
         const bool overlap = tile_base > 0 && !(dbg & kDebugNoOverlap);
         cudaLaunchAttribute attr[2];
@@ -491,6 +513,20 @@ int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, f
                                                  (float *)nullptr, 0, (int)tile_base, info.err_word, wait, dbg);
         return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
     }
+}
+
+// Launch the TMA kernel of tile T (see launch_tma_as); the main tile takes its
+// PLAIN form when alpha = 1 and beta = 0.
+template <class T>
+int launch_tma(const Problem &p, float alpha, float beta, bool vc, int splits, float *partials, int ldp,
+               int64_t tile_base, int64_t tiles, int cs, bool primary, cudaStream_t stream, const DeviceInfo &info) {
+    if constexpr (std::is_same_v<T, TmaTile>) {
+        if (alpha == 1.f && beta == 0.f)
+            return launch_tma_as<T, true>(p, alpha, beta, vc, splits, partials, ldp, tile_base, tiles, cs, primary,
+                                          stream, info);
+    }
+    return launch_tma_as<T, false>(p, alpha, beta, vc, splits, partials, ldp, tile_base, tiles, cs, primary, stream,
+                                   info);
 }
 
 // One k-step (K <= 32) with C's rows 16-byte aligned: the small-K tile unrolled
@@ -528,6 +564,29 @@ int launch_smallk_store(const Problem &p, float alpha, cudaStream_t stream, cons
     const int64_t tiles = (int64_t)((p.M + T::BM - 1) / T::BM) * ((p.N + T::BN - 1) / T::BN);
     sgemm::sgemm_ffma_tma_smallk_store_kernel<T><<<(unsigned)tiles, T::THREADS, S::SMEM_BYTES, stream>>>(
         ta, tb, tc, p.M, p.N, p.K, alpha, info.err_word, g_wait_limit_ns.load(), g_debug_flags.load());
+    return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
+}
+
+// One round of 128 x 64 tiles on the k-split kernel (ffma_tma_ksplit.cuh):
+// one CTA per tile, two groups of warps on alternate k-steps.
+int launch_ksplit(const Problem &p, float alpha, float beta, bool vc, int64_t tiles, cudaStream_t stream,
+                  const DeviceInfo &info) {
+    using T = TmaKSplit;
+    alignas(64) CUtensorMap ta, tb;
+    if (!encode_2d(&ta, p.A, p.M, p.K, p.lda, T::BM, T::BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tb, p.B, p.K, p.N, p.ldb, T::BK, T::BN, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return SGEMM_ERR_LAUNCH;
+    static std::atomic<int> done[kMaxDevices][4];
+    using sgemm::sgemm_ffma_tma_ksplit_kernel;
+    const bool plain = alpha == 1.f && beta == 0.f;
+    auto kernel = plain ? (vc ? sgemm_ffma_tma_ksplit_kernel<T, true, true>
+                              : sgemm_ffma_tma_ksplit_kernel<T, false, true>)
+                        : (vc ? sgemm_ffma_tma_ksplit_kernel<T, true, false>
+                              : sgemm_ffma_tma_ksplit_kernel<T, false, false>);
+    if (!smem_attr_once(done[info.dev][(vc ? 1 : 0) + (plain ? 2 : 0)], kernel, T::SMEM_BYTES)) return SGEMM_ERR_LAUNCH;
+    kernel<<<(unsigned)tiles, 2 * T::THREADS, T::SMEM_BYTES, stream>>>(ta, tb, p.M, p.N, p.K, alpha, beta, p.C, p.ldc,
+                                                                      info.err_word, g_wait_limit_ns.load(),
+                                                                      g_debug_flags.load());
     return cudaGetLastError() == cudaSuccess ? SGEMM_OK : SGEMM_ERR_LAUNCH;
 }
 
@@ -700,6 +759,7 @@ int launch_product(const Problem &p, int splits, float *partials, int ldp, cudaS
                           : phased ? Narrow::kPhased
                                    : (cp_narrow_fits(p) ? Narrow::kCp : Narrow::kNone);
     const SplitPlan plan = split_plan(p.M, p.N, p.K, info, narrow, phased);
+    if (plan.ksplit) return launch_ksplit(p, alpha, beta, vc, plan.tiles, stream, info);
     if (plan.narrow)
         return tma      ? launch_tma<TmaNarrow>(p, alpha, beta, vc, 1, partials, ldp, 0, plan.tiles, plan.cs, false,
                                                 stream, info)
@@ -794,7 +854,9 @@ StreamKPlan streamk_plan_model(int M, int N, int K, int64_t sms, int64_t residen
     const int64_t units = plan.tiles * ((K + T::BK - 1) / T::BK);
     if (!(dbg & kDebugForceStreamK)) {
         const SplitPlan sp = split_plan_model(M, N, K, sms, Narrow::kTma, dbg, fits);
-        const int64_t ctas = sp.narrow ? sp.tiles * sp.cs : sp.full + (sp.tiles - sp.full) * sp.cs;
+        // (the k-split plan fills at least 70 % of the SMs with one round of
+        // tiles, and beat stream-K there: 1024^3)
+        const int64_t ctas = sp.ksplit ? sms : sp.narrow ? sp.tiles * sp.cs : sp.full + (sp.tiles - sp.full) * sp.cs;
         const bool long_k = plan.tiles < sms && units >= kStreamKMinUnits * resident;
         if (ctas >= sms && !long_k) return plan;
     }

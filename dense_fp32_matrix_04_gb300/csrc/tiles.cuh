@@ -60,4 +60,16 @@ using TmaNarrowTile = TmaTile<8, 8, 2, 2, 2, 1, 4, 8, true>;
 // 2048 44.6 against 32.6, 1536^3 43.6 against 35.4, 512^3 14.9 against 7.5.
 using TmaNarrowCpTile = TmaTile<8, 8, 2, 2, 3, 1, 3, 8, true>;
 
+// One round of 128 x 64 tiles (70-100 % of the SM count, at most 48 k-steps)
+// on the TMA kernel of ffma_tma_ksplit.cuh: one CTA per tile of two groups of
+// two warps, each group taking one half of every k-step, 8 x 16 packed per
+// thread with the row walk, 3 stages.  This is the per-group tile.  Measured
+// against the narrow tile's cluster plan (us per product, CUDA events, mean of
+// 400 calls after an L2 flush): 1024^3 52.8 against 54.0, 1024 x 1216 x 1024
+// 52.8 against 64.3, 960^3 49.6 against 54.1, 1024 x 1024 x 512 30.7 against
+// 33.8; at 64 k-steps the cluster plan wins (1024 x 1024 x 2048: 95.5
+// against 97.7).  A variant whose groups took alternate k-steps (each with its
+// own two stages of a 4-stage ring) ran 4 % slower at 1024^3.
+using TmaKSplitTile = TmaTile<8, 16, 2, 1, 3, 1, 1, 4, true>;
+
 }  // namespace sgemm

@@ -53,7 +53,7 @@ def narrow_sm_time(model, L, w):
     return L * w / steps + rnd * -(-L // per_sm)
 
 
-def expected_plan(M, N, K, sms, narrow="tma"):
+def expected_plan(M, N, K, sms, narrow="tma", ksplit=False):
     """The automatic plan restated, as (tiles, full, cluster size, tile width):
     the 128 x 128 tiles beyond whole multiples of the SM count P (all of them
     when there are fewer than P) are split over the cluster size c = 2, 4 or 8
@@ -64,7 +64,9 @@ def expected_plan(M, N, K, sms, narrow="tma"):
     the plain grid by 4 %.  With fewer tiles than P, 128 x 64 narrow tiles of
     the path (`narrow`: "tma", "cp" or None) in clusters of c = 2, 4 or 8 (the
     lowest estimate of that path's NARROW_MODEL, ties to the larger c) replace
-    that when lower still."""
+    that when lower still; on the TMA path (`ksplit`), narrow tiles that fill
+    at least 70 % of one round over the SMs with at most 48 k-steps take the
+    k-split tile instead, one CTA per tile (cluster size 1, every tile full)."""
     P = sms
     tiles = -(-M // 128) * -(-N // 128)
     rem = tiles % P
@@ -84,6 +86,8 @@ def expected_plan(M, N, K, sms, narrow="tma"):
             cs, best = 1, plain
         if narrow and tiles < P:
             ntiles = -(-M // 128) * -(-N // 64)
+            if ksplit and ntiles <= P and 100 * ntiles >= 70 * P and kt <= 48:
+                return (ntiles, ntiles, 1, 64)
             ncs, nbest = 0, 0.0
             for c in (2, 4, 8):
                 if kt < 4 * c:
@@ -146,7 +150,7 @@ def test_tail_split_after_full_waves(sg, overlap):
     M, N, K = 128 * tiles_m - 37, 128 * tiles_n - 4, 1000   # N % 4 == 0: the TMA path
     A, B = gen.operands(M, N, K, seed=207)
     tiles, full, cs, tn = sg.sgemm_f32_plan(M, N, K)
-    assert (tiles, full, cs, tn) == expected_plan(M, N, K, sms)
+    assert (tiles, full, cs, tn) == expected_plan(M, N, K, sms, ksplit=True)
     assert cs > 1 and 0 < full < tiles and tn == 128
     C = run_sgemm(sg, A, B)
     rows = [0, 1, 127, 128, M - 129, M - 128, M - 2, M - 1] + list(np.random.default_rng(1).integers(0, M, 12))
@@ -159,7 +163,7 @@ def test_tail_split_after_full_waves(sg, overlap):
 def test_automatic_plan(sg, M, N, K):
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms)
+    assert sg.sgemm_f32_plan(M, N, K) == expected_plan(M, N, K, sms, ksplit=True)
     # operands the TMA cannot address directly: the phased TMA kernel, whose
     # narrow tile runs like the TMA kernel's (four CTAs per SM) and takes its model
     assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow="tma")
@@ -171,9 +175,10 @@ def test_automatic_plan(sg, M, N, K):
     assert sg.sgemm_f32_plan(M, N, K, aligned=False) == expected_plan(M, N, K, sms, narrow=None)
 
 
-def test_square_1024_uses_clusters_and_matches(sg):
-    A, B = gen.operands(1024, 1024, 1024, seed=1)
-    assert sg.sgemm_f32_plan(1024, 1024, 1024)[2] > 1
+def test_square_768_uses_clusters_and_matches(sg):
+    # (1024^3 takes the k-split tile, tested in test_ksplit_gpu.py)
+    A, B = gen.operands(768, 768, 768, seed=1)
+    assert sg.sgemm_f32_plan(768, 768, 768)[2] > 1
     check_full(run_sgemm(sg, A, B), A, B)
 
 

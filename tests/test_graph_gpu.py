@@ -36,7 +36,8 @@ def _buffers(torch, M, N, K, aligned):
 
 @pytest.mark.parametrize("M,N,K,aligned,expect", [
     (8192, 2048, 512, True, "plain"),            # 1024 tiles: no split
-    (1024, 1024, 1024, True, "split"),           # every tile in clusters
+    (768, 1024, 2048, True, "split"),            # every tile in clusters
+    (1024, 1024, 1024, True, "ksplit"),          # one round of tiles, two warp groups per tile
     (2048, 2048, 2048, True, "plain+split"),     # primary grid + overlapped clusters
     (3001, 4999, 2047, False, "phased"),         # unaligned: phase maps, with a cluster tail
     (3, 2000, 1001, False, "cp.async"),          # unaligned, three rows of A: cp.async-fed
@@ -49,6 +50,8 @@ def test_sgemm_f32_replays_bitwise(sg, M, N, K, aligned, expect):
         assert cs > 1 and full == 0
     if expect == "plain+split":
         assert cs > 1 and 0 < full < tiles
+    if expect == "ksplit":
+        assert (full, cs, tn) == (tiles, 1, 64)
     A, B, C = _buffers(torch, M, N, K, aligned)
     a0, b0 = gen.operands(M, N, K, seed=400)
     A.copy_(torch.from_numpy(a0))

@@ -39,7 +39,7 @@ def narrow_plan(sg, M, N, K, aligned=True):
     return cs
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (512, 512, 4096), (1024, 1024, 1024), (257, 130, 1000),
+@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (512, 512, 4096), (768, 768, 768), (257, 130, 1000),
                                    (640, 640, 8192), (1000, 200, 777), (129, 65, 2000)])
 def test_matches_oracle(sg, M, N, K):
     # leading dimensions padded to 4 floats keep every case on the TMA path
@@ -79,7 +79,7 @@ def test_against_the_wide_tile(sg):
     # the two tiles divide the k-steps differently, so they agree within the
     # bound, not bit for bit; switching the narrow tile off restores the wide one
     import torch
-    M, N, K = 1024, 1024, 1024
+    M, N, K = 768, 1024, 2048
     narrow_plan(sg, M, N, K)
     A, B = gen.operands(M, N, K, seed=622)
     c_narrow = run_sgemm(sg, A, B)

@@ -92,6 +92,10 @@ def test_narrow_tile_choice_matches_the_measurements(path, row):
     M, N, K, wide, narrow = row
     assert tiles128(M, N) < SMS
     tiles, full, cs, tile_n = sg.sgemm_f32_plan_model(M, N, K, SMS, path)
+    if (tile_n, cs, full) == (64, 1, tiles):
+        # the k-split tile, checked against its own measurements below
+        assert path == "tma" and (M, N, K) in {r[:3] for r in KSPLIT_MEASURED}
+        return
     picked = narrow if tile_n == 64 else wide
     assert picked >= (1 - NEAR) * max(wide, narrow), (
         f"{M}x{N}x{K} on {path}: planned {'narrow' if tile_n == 64 else '128x128'} ({picked} TF/s) "
@@ -99,6 +103,48 @@ def test_narrow_tile_choice_matches_the_measurements(path, row):
     if tile_n == 64:
         # the narrow tile always runs as clusters that split each tile's k-steps
         assert full == 0 and cs in (2, 4, 8) and tiles == -(-M // 128) * -(-N // 64)
+
+
+# One round of 128 x 64 tiles: the narrow tile's cluster plan against the
+# k-split tile (one CTA per tile, two warp groups on the two halves of every
+# k-step), us per product (CUDA events, mean of 400 calls after an L2 flush),
+# and whether the k-split tile is the plan (at least 70 % of the SMs filled,
+# at most 48 k-steps).
+KSPLIT_MEASURED = [
+    # M, N, K, cluster plan us, k-split us, taken
+    (1024, 1024, 512, 33.8, 30.7, True),
+    (1024, 1024, 1024, 54.0, 52.8, True),
+    (1024, 1024, 1536, 76.0, 75.3, True),
+    (1024, 1216, 1024, 64.3, 52.8, True),
+    (896, 1024, 1024, 53.9, 52.7, True),
+    (800, 1024, 1024, 53.9, 52.8, True),
+    (1000, 1000, 1000, 54.1, 52.9, True),
+    (1152, 1024, 1024, 55.1, 52.8, True),
+    (960, 960, 960, 54.1, 49.6, True),
+    (1280, 960, 1024, 64.3, 52.9, True),
+    (1024, 1024, 2048, 95.5, 97.7, False),
+    (1024, 1152, 2048, 96.3, 97.9, False),
+    (1024, 1024, 4096, 176.9, 182.6, False),
+    (768, 1024, 2048, 75.3, 94.5, False),
+    (640, 1024, 4096, 115.0, 182.6, False),
+    (512, 1024, 8192, 178.7, 357.0, False),
+]
+
+
+@pytest.mark.parametrize("M,N,K,cluster_us,ksplit_us,taken", KSPLIT_MEASURED)
+def test_ksplit_tile_where_measured_faster(M, N, K, cluster_us, ksplit_us, taken):
+    tiles, full, cs, tile_n = sg.sgemm_f32_plan_model(M, N, K, SMS, "tma")
+    ntiles = -(-M // 128) * -(-N // 64)
+    if taken:
+        assert ksplit_us <= (1 + NEAR) * cluster_us
+        assert (tiles, full, cs, tile_n) == (ntiles, ntiles, 1, 64)
+    else:
+        assert cluster_us <= (1 + NEAR) * ksplit_us
+        assert tile_n != 64 or cs > 1
+    # only the TMA path has the k-split tile
+    for path in ("phased", "cp"):
+        t, f, c, n = sg.sgemm_f32_plan_model(M, N, K, SMS, path)
+        assert not (n == 64 and c == 1)
 
 
 def test_narrow_tile_needs_fewer_main_tiles_than_sms():
@@ -244,4 +290,5 @@ def test_streamk_limits():
     import ctypes
     b, w = ctypes.c_longlong(), ctypes.c_size_t()
     for args in [(-1, 4, 4, SMS, 2), (4, 4, 4, 0, 2), (4, 4, 4, SMS, 0)]:
-        assert sg.load().sgemm_f32_streamk_plan_model(*args, ctypes.byref(b), ctypes.byref(w)) == sg.SGEMM_ERR_INVALID_ARG
+        st = sg.load().sgemm_f32_streamk_plan_model(*args, ctypes.byref(b), ctypes.byref(w))
+        assert st == sg.SGEMM_ERR_INVALID_ARG
