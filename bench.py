@@ -68,7 +68,8 @@ TRAFFIC_PROFILES = {
     "skinny_16384x16384x32": ("ffma_tma_skinny_16384x16384x32.md",
                               ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_smallk.cuh"] + KERNEL_SOURCES,
                               "TmaSmallKStoreTile"),
-    "square_1024": ("ffma_narrow_square_1024.md", KERNEL_SOURCES, "TmaNarrowTile"),
+    "square_1024": ("ffma_ksplit_square_1024.md", ["dense_fp32_matrix_04_gb300/csrc/ffma_tma_ksplit.cuh"] + KERNEL_SOURCES,
+                    "TmaKSplitTile"),
     "square_16384": ("ffma_tma_square_16384.md", KERNEL_SOURCES, "TmaMainTile"),
     "tiny_6x6x9": ("ffma_tiny_6x6x9.md", ["dense_fp32_matrix_04_gb300/csrc/ffma_tiny.cuh",
                                           "dense_fp32_matrix_04_gb300/csrc/epilogue.cuh"], None),

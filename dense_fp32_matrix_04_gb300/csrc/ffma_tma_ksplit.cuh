@@ -29,48 +29,15 @@
 
 namespace sgemm {
 
-// Groups [g0, g0 + GN) of four k-values of one 32-deep stage, for this
-// thread's TM x TN block, as packed column pairs (column-pair outer, the rows
-// walked down and up in turn): the arithmetic of tile_fma's packed form over a
-// part of the stage.  A rows at `sa` (128-byte rows, 128-byte swizzle: the
-// thread's rows are lm + 8 i), B row segments at `sb`.  Written out here
-// rather than shared with tile_fma: this form, with the group offset a
-// runtime value, measured 7 % faster in this kernel (1024^3: 50.8 against
-// 54.9 us).
-template <class T, int GN>
-__device__ __forceinline__ void half_fma(uint64_t (&acc2)[T::TM][T::TN / 2], const unsigned char *sa,
-                                         const unsigned char *sb, int lm, int g0) {
-#pragma unroll
-    for (int gg = 0; gg < GN; ++gg) {
-        const int g = g0 + gg;
-        const unsigned char *ag = sa + ((g ^ lm) << 4);
-        float4 a[T::TM];
-#pragma unroll
-        for (int i = 0; i < T::TM; ++i) a[i] = *reinterpret_cast<const float4 *>(ag + 1024 * i);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const unsigned char *bk = sb + (4 * g + kk) * (T::BN * 4);
-            uint64_t b2[T::TN / 2];
-#pragma unroll
-            for (int q = 0; q < T::TN / 4; ++q) {
-                const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(bk + 64 * q);
-                b2[2 * q] = v.x;
-                b2[2 * q + 1] = v.y;
-            }
-            uint64_t ad[T::TM];
-#pragma unroll
-            for (int i = 0; i < T::TM; ++i)
-                ad[i] = f32x2_dup(kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w);
-#pragma unroll
-            for (int j = 0; j < T::TN / 2; ++j)
-#pragma unroll
-                for (int ii = 0; ii < T::TM; ++ii) {
-                    const int i = (j & 1) ? T::TM - 1 - ii : ii;
-                    f32x2_fma(acc2[i][j], ad[i], b2[j]);
-                }
-        }
-    }
-}
+// The tile T seen by one group: half of each 32-deep k-step, four groups of
+// four k-values (tile_fma walks BK / 4 of them, all unrolled).  The second
+// half starts 16 rows into the B stage, and its A chunks 4..7 of a row sit at
+// chunk (4 + g) ^ (r % 8) = g ^ ((r % 8) ^ 4) of the 128-byte swizzle, so that
+// group passes lm ^ 4 where the first passes lm.
+template <class T>
+struct HalfK : T {
+    static constexpr int BK = T::BK / 2, G_UNROLL = T::BK / 8;
+};
 
 // T: the per-group tile (two warps, 128 x 64, packed); the CTA runs 2 * T::THREADS threads.
 // PLAIN: alpha = 1 and beta = 0 (C = A B, the arguments are not read), known
@@ -82,7 +49,7 @@ __global__ void __launch_bounds__(2 * T::THREADS, 1)
                                  int M, int N, int K, float alpha, float beta, float *__restrict__ C, int ldc,
                                  int *__restrict__ err_word, unsigned long long wait_limit_ns, int debug) {
     static_assert(T::PACKED, "group 1 hands over packed accumulators");
-    static_assert(T::BK == 32, "two halves of four 4-deep k-groups of a 128-byte A row");
+    static_assert(T::BK == 32, "two halves of four 4-deep k-groups; chunks 4..7 of a 128-byte row");
     static_assert(T::TM * T::TN * T::THREADS * 4 <= T::STAGES * T::STAGE, "group 1 parks its sums in the stages");
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -131,20 +98,23 @@ __global__ void __launch_bounds__(2 * T::THREADS, 1)
     const int row0 = (warp / T::WARPS_N) * T::WM + lm;
     const int col0 = (warp % T::WARPS_N) * T::WN + ln * 4;
 
+    float acc[1][1];  // unused: the packed form keeps acc2
     uint64_t acc2[T::TM][T::TN / 2];
 #pragma unroll
     for (int i = 0; i < T::TM; ++i)
 #pragma unroll
         for (int j = 0; j < T::TN / 2; ++j) acc2[i][j] = 0ull;
 
-    constexpr int HALF = T::BK / 8;  // four-deep k-groups per half of a stage
+    // this group's half of every k-step: B rows 16 * group on, A chunks through lm ^ (4 * group)
+    const int lm_half = lm ^ (4 * group);
+    const int b_half = group * (T::BK / 2) * (T::BN * 4);
     int failed_k0 = -1;
     for (int kt = 0; kt < KT; ++kt) {
         const int s = kt % T::STAGES;
         const bool ok = mbar_wait_bounded(bars + 8 * s, (kt / T::STAGES) & 1, wait_limit_ns);
         if (ok) {
             const unsigned char *stage = smem + s * T::STAGE;
-            half_fma<T, HALF>(acc2, stage + row0 * 128, stage + T::A_STAGE + col0 * 4, lm, group * HALF);
+            tile_fma<HalfK<T>>(acc, acc2, stage + row0 * 128, stage + T::A_STAGE + b_half + col0 * 4, lm_half);
         }
         // both groups are done with stage s (or give up together)
         if (__syncthreads_or(!ok)) {
@@ -187,7 +157,6 @@ __global__ void __launch_bounds__(2 * T::THREADS, 1)
             f32x2_fma(acc2[i][2 * q], v.x, one2);  // s + v, rounded once (v * 1 is exact)
             f32x2_fma(acc2[i][2 * q + 1], v.y, one2);
         }
-    float acc[1][1];  // unused: the packed form keeps acc2
     store_tile<T, VEC_C, false>(acc, acc2, C, ldc, M, N, m0 + row0, n0 + col0, PLAIN ? 1.f : alpha, PLAIN ? 0.f : beta,
                                 1, 0);
 }

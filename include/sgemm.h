@@ -99,7 +99,11 @@ typedef enum {
  * thread; four blocks per SM on the TMA and phased paths, three on the
  * cp.async path, the latter only when 16 * lda and 8 * ldb fit in 32 bits),
  * all in such clusters
- * (sgemm_f32_plan reports the choice).  Tiny products -- at most 16384
+ * (sgemm_f32_plan reports the choice).  On the TMA path, products whose
+ * narrow tiles fill one round over the SMs to at least 70 % with at most 48
+ * k-steps (e.g. 1024^3) instead run one block per narrow tile, of two groups
+ * of warps that each take one half of every k-step and add their sums in
+ * shared memory (no cluster).  Tiny products -- at most 16384
  * outputs, 1 <= K <= 128, on any path -- skip the tiles: one thread per output
  * computes its dot product straight from memory (the pages' naive kernel),
  * which for them costs a fraction of the tiled kernels' set-up.
@@ -124,7 +128,8 @@ int sgemm_f32(int M, int N, int K,
  * *full_tiles == *tiles).  *tile_n is 64 for TMA operands with 1 <= K <= 64
  * (never split) and for the narrow tile, which a product with fewer 128 x 128
  * tiles than SMs takes when its cost model says so (then every tile is in a
- * cluster); 128 otherwise.  Non-TMA operands with M >= 4 and K >= 4 take the
+ * cluster, or, for the two-group k-split blocks of TMA operands,
+ * *cluster_size == 1 and *full_tiles == *tiles); 128 otherwise.  Non-TMA operands with M >= 4 and K >= 4 take the
  * phased TMA kernel's plan; smaller ones the cp.async kernel's, which assumes
  * 16 * lda and 8 * ldb fit in 32 bits (otherwise the 128 x 128 plan runs).  The result
  * reflects the switches of the test-only interface (sgemm_testing.h), which
