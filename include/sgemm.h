@@ -280,7 +280,7 @@ size_t sgemm_f32_3xtf32_workspace_size(int M, int N, int K);
  * the whole device-memory budget (a plug-in handed only its input and output
  * buffers), or a latency-critical loop where an allocation, which may
  * synchronise the device and take unbounded time, is not allowed.  The
- * surveyed pages have no counterpart to this entry point; it only changes
+ * SGEMM pages have no counterpart to this entry point; it only changes
  * where the split-K partial products live.
  *
  * The partials go to one fixed array in device memory that the library
