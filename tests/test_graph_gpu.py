@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import gen
+from helpers import check_full
 
 pytestmark = pytest.mark.gpu
 
@@ -130,4 +131,41 @@ def test_splitk_3xtf32_and_gemm_replay_bitwise(sg):
     assert torch.equal(got, C) and torch.equal(got3, C3)
     for algo in (0, 1):
         assert torch.equal(got_g[algo], Cg[algo])
+    assert sg.sgemm_device_status() == sg.SGEMM_OK
+
+
+def test_streamk_replays_bitwise(sg):
+    # the stream-K kernel is a cooperative launch after a memset of its tile
+    # counters: both are captured, and a replay gives the eager call's bits
+    import torch
+    M, N, K = 256, 256, 16384
+    A, B, C = _buffers(torch, M, N, K, True)
+    need = sg.sgemm_f32_streamk_workspace_size(M, N, K)
+    assert need > 0
+    ws = torch.empty(need // 4, device="cuda")
+    a0, b0 = gen.operands(M, N, K, seed=405)
+    A.copy_(torch.from_numpy(a0))
+    B.copy_(torch.from_numpy(b0))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sg.matmul_streamk(A, B, out=C, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sg.matmul_streamk(A, B, out=C, workspace=ws)
+    for seed in (406, 407):
+        a, b = gen.operands(M, N, K, seed=seed)
+        A.copy_(torch.from_numpy(a))
+        B.copy_(torch.from_numpy(b))
+        C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        got = C.clone()
+        C.fill_(float("nan"))
+        sg.matmul_streamk(A, B, out=C, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, C)
+        check_full(got.cpu().numpy(), a, b)
     assert sg.sgemm_device_status() == sg.SGEMM_OK
