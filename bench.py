@@ -13,12 +13,20 @@ flush is needed between steps.
 * ``value``: TFLOP/s = 2MNK * steps * ranks / (max over ranks of the device
   time of the K timed steps), inputs resident in HBM.
 * ``e2e``: the same metric through the public call with host buffers: each
-  step copies A and B from pinned host memory, runs sgemm_f32 and copies C back.
+  step copies A and B from pinned host memory, runs sgemm_f32 and copies C back
+  (sgemm_f32_host, copies overlapped with the product); the median of three
+  rounds of --e2e-steps calls, every round listed.
 * ``roofline``: the kernel is bound by the FP32 FFMA pipes.  Peak =
   SMs x 128 FP32 lanes x 2 FLOP x clock, at the maximum SM clock (2070 MHz)
   and, beside it, at the median clock sampled during the timed region.
 * ``cpu_baseline``: the CPU oracle (FP64 triple loop) on a bounded sample of the
   rows of the same product, on this host's cores.
+* ``variants``: the same product through sgemm_f32_3xtf32 (tensor cores).
+* ``configs``: every other workload (6x6x9, 1024^3, 3001x4999x2047,
+  16384^2x32, 16384^3, 256x256x65536), each through sgemm_f32 over about two
+  seconds of steps with its own clock samples, roofline, DRAM bytes from its
+  committed ncu summary, sampled oracle check and end-to-end figure; with the
+  3xTF32 and stream-K entry points beside it where they apply.
 
 Under torchrun (N > 1) each rank runs its own full replica of the product
 (one process per GPU, no collective on the data path); ``--impl reference``
