@@ -199,8 +199,9 @@ int sgemm_f32_splitk_suggest(int M, int N, int K, int *splits);
  *   Stream-K runs when A and B are 16-byte aligned with leading dimensions
  *   that are multiples of 4, K > 64, the product is not a tiny one (see
  *   sgemm_f32), and either sgemm_f32's own plan would start fewer blocks than
- *   the device has SMs, or there are fewer 128 x 128 tiles than SMs and each
- *   block gets at least 24 units.  Every other product runs exactly as
+ *   the device has SMs (its one-round k-split blocks count as filling them),
+ *   or there are fewer 128 x 128 tiles than SMs and each block gets at least
+ *   24 units.  Every other product runs exactly as
  *   sgemm_f32 does and reads no workspace.  The kernel is launched
  *   cooperatively (all of its blocks resident at once).
  *   workspace: caller-owned device memory of at least
